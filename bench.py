@@ -1,0 +1,512 @@
+#!/usr/bin/env python
+"""Benchmark of the block-verification hot path on GB300.
+
+Headline: verified rows/s and achieved HBM GB/s of the W4 verify projection
+at M=8, K=5120, N=17408 (bf16 activations, group-64 affine 4-bit weights).
+One step = one vq_linear call on one verify block of 8 rows. Prints one JSON
+line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed steps, then exactly K steps replayed from CUDA graphs on one
+stream, bracketed by a barrier and torch.cuda.synchronize(), CUDA events on
+that stream; the max over ranks is reported. The weights rotate over enough
+copies (11 x 50.5 MB = 555 MB) that every step reads them from HBM, not L2.
+`e2e` is the same metric through the public binding with the activations
+copied in from pinned host memory and the result copied back every step.
+`--impl reference` times the CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "verified rows/s and HBM GB/s (% of peak), W4 M=8 K=5120 N=17408 verify GEMM"
+WORKLOAD = "verify_w4_m8_k5120_n17408"
+M, K, N = 8, 5120, 17408
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20
+
+
+def alg_bytes(M, K, N, x_bytes=2, y_bytes=2):
+    """Weights once, scales and biases once, x once, y once."""
+    return K * N // 2 + 2 * 2 * N * (K // 64) + M * K * x_bytes + M * N * y_bytes
+
+
+CONFIG = {
+    "workload": WORKLOAD, "M": M, "K": K, "N": N, "activations": "bf16 ~N(0,1)",
+    "weights": "W4 group-64 affine, codes U{0..15}, bf16 scale U(0.005,0.02), bias U(-0.1,0.1)",
+    "seed": 0,
+}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-path", action="store_true", help="skip the per-kernel path table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            for key in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if key in d and d[key]:
+                    return float(d[key]), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest() -> str:
+    """sha256 over the CUDA sources: ties a profile's counters to this code."""
+    csrc = os.path.join(ROOT, "speculative_block_draft_02_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_tag: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current sources (else None)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    digest = source_digest()
+    for name in sorted(os.listdir(pdir)):
+        if kernel_tag not in name:
+            continue
+        text = open(os.path.join(pdir, name)).read()
+        m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+        d = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+        if m and d and d.group(1) == digest:
+            return int(m.group(1))
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        ident = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        # samples under load: the SM clock is at its running value while busy
+        busy = sorted(sm)[len(sm) // 2:] if sm else []
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def dev_weights(seed, n_copies, N_, K_):
+    from speculative_block_draft_02_gb300 import synth
+
+    w = synth.w4_weights(seed, N_, K_)
+    qw = torch.from_numpy(w.qw.view(np.int32).copy())
+    s = torch.from_numpy(w.scales.view(np.int16).copy())
+    b = torch.from_numpy(w.biases.view(np.int16).copy())
+    copies = [(qw.cuda(), s.cuda(), b.cuda()) for _ in range(n_copies)]
+    return w, copies
+
+
+def dev_act(seed, M_, K_, dtype="bf16", scale=1.0, name="x"):
+    from speculative_block_draft_02_gb300 import synth
+
+    xb = synth.activations(seed, M_, K_, dtype, scale=scale, name=name)
+    if dtype == "f32":
+        return xb, torch.from_numpy(xb).cuda()
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+    return xb, torch.from_numpy(xb.view(np.int16).copy()).view(tdt).cuda()
+
+
+def n_copies_for(bytes_per_copy):
+    return max(2, -(-4 * L2_BYTES // bytes_per_copy))
+
+
+def graph_of(calls):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    return g
+
+
+def time_calls(calls, steps, warmup, world=1, per_graph=220):
+    """Run `steps` calls (cycling through `calls`) from CUDA graphs; returns
+    (total seconds over ranks, per-launch seconds)."""
+    for i in range(max(warmup, len(calls))):
+        calls[i % len(calls)]()
+    torch.cuda.synchronize()
+    P = min(steps, per_graph)
+    body = graph_of([calls[i % len(calls)] for i in range(P)])
+    reps, tail_n = divmod(steps, P)
+    tail = graph_of([calls[i % len(calls)] for i in range(tail_n)]) if tail_n else None
+    body.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    barrier(world)
+    torch.cuda.synchronize()
+    ev[0].record(stream)
+    for _ in range(reps):
+        body.replay()
+    if tail is not None:
+        tail.replay()
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t = ev[0].elapsed_time(ev[1]) / 1e3
+    return max_over_ranks(t, world), t / steps
+
+
+def run_ours(args):
+    from speculative_block_draft_02_gb300 import binding as vq
+    from speculative_block_draft_02_gb300 import build
+
+    rank, world, local = dist_setup()
+    build.build()
+    vq.lib()
+    dev = torch.cuda.current_device()
+    K_steps, W = args.steps, max(3, args.warmup)
+
+    # ---- headline: vq_linear M=8 K=5120 N=17408 bf16, rotating weight copies
+    b_main = alg_bytes(M, K, N)
+    n_cp = n_copies_for(b_main)
+    w, copies = dev_weights(0, n_cp, N, K)
+    xb, x = dev_act(0, M, K)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    assert vq.vq_linear_workspace_bytes(M, K, N) == 0
+    calls = [(lambda c=c: vq.vq_linear(x, *c, y=y)) for c in copies]
+
+    clocks = ClockSampler(dev)
+    total, per_launch = time_calls(calls, K_steps, W, world)
+    clk = clocks.stop()
+
+    rows_per_s = world * M * K_steps / total
+    peak, peak_kind = measured_peaks()
+    achieved = b_main / per_launch / 1e9
+    traffic = profiled_traffic("vq_linear_bf16_m8_k5120_n17408")
+
+    # ---- e2e through the public binding, host buffers, copies every step
+    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_host.copy_(x)
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_dev = torch.empty_like(x)
+    e2e_steps = K_steps
+    for i in range(W):
+        x_dev.copy_(x_host, non_blocking=True)
+        vq.vq_linear(x_dev, *copies[i % n_cp], y=y)
+        y_host.copy_(y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        vq.vq_linear(x_dev, *copies[i % n_cp], y=y)
+        y_host.copy_(y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+    e2e = {"value": world * M * e2e_steps / t_e2e, "unit": "rows/s",
+           "h2d_bytes_per_step": x.numel() * x.element_size(),
+           "d2h_bytes_per_step": y.numel() * y.element_size(),
+           "us_per_step": t_e2e / e2e_steps * 1e6}
+
+    line = {
+        "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world,
+        "steps": K_steps, "warmup": W, "ms_per_step": total / K_steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": dict(CONFIG, parallelism="replicas" if world > 1 else "single",
+                       l2="inputs > L2: %d rotating weight copies (%.0f MB)"
+                          % (n_cp, n_cp * b_main / 1e6),
+                       timing="CUDA graphs of %d launches, events on the launch stream"
+                              % min(K_steps, 220)),
+        "hbm_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": b_main, "kernel": "vq_gemm_kernel<bf16,MT=1>",
+                     "us_per_launch": per_launch * 1e6},
+        "e2e": e2e, "gpu_launches": K_steps, "clocks": clk,
+    }
+
+    if not args.no_path:
+        line["path"] = path_table(vq, copies, x, W, world)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline_full(w, xb)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def path_table(vq, copies, x, W, world):
+    """Every other step of the hot path, each at its own workload, timed the
+    same way (fewer launches): microseconds per launch and algorithmic GB/s."""
+    from speculative_block_draft_02_gb300 import synth
+
+    out = {}
+    steps = 400
+
+    def record(name, calls, nbytes, rows=None, n=steps):
+        total, per = time_calls(calls, n, 20, world)
+        d = {"us": per * 1e6, "alg_bytes": nbytes, "gbs": nbytes / per / 1e9 if nbytes else None}
+        if rows:
+            d["rows_per_s"] = rows / per
+        out[name] = d
+
+    # narrow output (the pages' N=1024 case) and the block-size / dtype sweep
+    w1, c1 = dev_weights(0, n_copies_for(alg_bytes(8, K, 1024)), 1024, K)
+    for Mi in (4, 8):
+        _, xi = dev_act(0, Mi, K, "bf16", 0.5)
+        yi = torch.empty((Mi, 1024), dtype=torch.bfloat16, device="cuda")
+        wsi = torch.zeros(max(vq.vq_linear_workspace_bytes(Mi, K, 1024), 16), dtype=torch.uint8,
+                          device="cuda")
+        record("verify_m%d_k5120_n1024_bf16" % Mi,
+               [(lambda c=c, xi=xi, yi=yi, wsi=wsi: vq.vq_linear(xi, *c, y=yi, workspace=wsi))
+                for c in c1], alg_bytes(Mi, K, 1024), rows=Mi)
+    out["ratio_m8_over_m4_rows_n1024"] = (out["verify_m8_k5120_n1024_bf16"]["rows_per_s"] /
+                                          out["verify_m4_k5120_n1024_bf16"]["rows_per_s"])
+    del c1
+    for dt in ("bf16", "f16", "f32"):
+        for Mi in (1, 4, 8, 16):
+            _, xi = dev_act(0, Mi, K, dt, 0.5)
+            yi = torch.empty((Mi, N), dtype=xi.dtype, device="cuda")
+            eb = 4 if dt == "f32" else 2
+            record("verify_m%d_k5120_n17408_%s" % (Mi, dt),
+                   [(lambda c=c, xi=xi, yi=yi: vq.vq_linear(xi, *c, y=yi)) for c in copies],
+                   alg_bytes(Mi, K, N, eb, eb), rows=Mi)
+        out["ratio_m8_over_m4_rows_n17408_%s" % dt] = (
+            out["verify_m8_k5120_n17408_%s" % dt]["rows_per_s"] /
+            out["verify_m4_k5120_n17408_%s" % dt]["rows_per_s"])
+
+    # next-block verify at M=64 (B=4 x block 16)
+    _, x64 = dev_act(0, 64, K, "bf16", name="x_next")
+    y64 = torch.empty((64, N), dtype=torch.bfloat16, device="cuda")
+    record("verify_m64_k5120_n17408_bf16",
+           [(lambda c=c: vq.vq_linear(x64, *c, y=y64)) for c in copies], alg_bytes(64, K, N),
+           rows=64, n=100)
+
+    # vocab projection + fused arg max, M=64, K=2560, N=151936
+    Kv, Nv, Mv = 2560, 151936, 64
+    bv = Kv * Nv // 2 + 4 * Nv * (Kv // 64) + Mv * Kv * 2 + Mv * 4
+    wv, cv = dev_weights(0, 2, Nv, Kv)
+    _, xv = dev_act(0, Mv, Kv)
+    wsv = torch.zeros(vq.vq_vocab_argmax_workspace_bytes(Mv), dtype=torch.uint8, device="cuda")
+    am = torch.empty(Mv, dtype=torch.int32, device="cuda")
+    record("vocab_argmax_m64_k2560_n151936_bf16",
+           [(lambda c=c: vq.vq_vocab_argmax(xv, *c, wsv, argmax=am)) for c in cv], bv, rows=Mv,
+           n=100)
+    del cv
+
+    # accept walk B=4 x L=16 and the per-row KV commit (8 layers x K,V)
+    tgt = torch.randint(0, Nv, (4, 16), dtype=torch.int32, device="cuda")
+    dft = tgt.clone()
+    acc = torch.empty(4, dtype=torch.int32, device="cuda")
+    record("accept_walk_b4_l16", [lambda: vq.verify_accept_walk(dft, tgt, accept=acc)],
+           2 * 4 * 16 * 4 + 16)
+    case = synth.commit_case(0)
+    kv = [torch.from_numpy(t.view(np.int16).copy()).cuda() for t in case.tensors]
+    i32 = lambda a: torch.from_numpy(np.asarray(a, dtype=np.int32)).cuda()
+    pl, so = i32(case.prefix_len), i32(case.src_off)
+    keep = i32(case.keep)
+    nl = torch.empty(4, dtype=torch.int32, device="cuda")
+    # every repetition moves the same slots (contents aside), so the cost per
+    # launch is that of one commit
+    moved = int(case.keep.sum()) * 8 * 128 * 2 * len(kv)
+    record("kv_commit_8layers_b4_h8_d128_fp16",
+           [lambda: vq.kv_compact_per_row(kv, pl, so, keep, 16, new_len=nl)], 2 * moved)
+    return out
+
+
+def cpu_baseline_full(w, xb, budget_s=12.0):
+    import oracle
+
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16)
+    t1 = time.perf_counter() - t0
+    reps = max(1, int(budget_s / max(t1, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16)
+    t = time.perf_counter() - t0
+    return {"value": M * reps / t, "unit": "rows/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "full M=8 K=5120 N=17408 bf16 step, %d repeats, fp64 scalar C, OpenMP over"
+                      " output columns" % reps}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+
+def run_reference(args):
+    import oracle
+    from speculative_block_draft_02_gb300 import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    oracle.build()
+    w = synth.w4_weights(0, N, K)
+    xb = synth.activations(0, M, K, "bf16")
+    # calibrate: columns per second on this host
+    cal = np.arange(0, 512, dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16, cols=cal)
+    t_col = (time.perf_counter() - t0) / len(cal)
+    steps, W = args.steps, max(3, args.warmup)
+    budget = 60.0
+    cols_per_step = int(min(N, max(16, budget / (steps + W) / max(t_col, 1e-9))))
+    starts = np.arange(0, N, cols_per_step)
+
+    def step(i):
+        c0 = int(starts[i % len(starts)])
+        cols = np.arange(c0, min(N, c0 + cols_per_step), dtype=np.int32)
+        oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16, cols=cols)
+        return len(cols)
+
+    for i in range(W):
+        step(i)
+    done = 0
+    t0 = time.perf_counter()
+    for i in range(steps):
+        done += step(i)
+    t = time.perf_counter() - t0
+    # rows/s of the full-N step: each verified row needs all N columns
+    value = M * (done / N) / t
+    sample = ("%d output columns of N=%d per step (all M=8 rows, K=5120), fp64 scalar C oracle"
+              % (cols_per_step, N))
+    cores = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": world, "steps": steps, "warmup": W, "ms_per_step": t / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": dict(CONFIG, parallelism="host cores"),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * vq.h -- C ABI of the GB300 (sm_103a) block-verification hot path.
+ *
+ * Four operations make up one verify round of DFlash-style block speculative
+ * decoding once the target has produced its hidden states:
+ *
+ *   vq_linear            the small-M verification projection over 4-bit
+ *                        group-quantized weights
+ *   vq_vocab_argmax      the vocabulary projection with the greedy arg max
+ *                        fused in (no logits are written)
+ *   verify_accept_walk   the per-row accept walk
+ *   kv_compact_per_row   the per-row KV commit
+ *
+ * Common rules
+ *   - Every tensor pointer is caller-owned DEVICE memory unless a parameter
+ *     says otherwise. The library allocates nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Every call only enqueues work on it and returns without
+ *     synchronizing; results are ready when the stream reaches that point.
+ *   - Calls return VQ_OK (0) or a negative VQ_E* code. Argument errors are
+ *     found on the host before anything is enqueued. Failures found on the
+ *     device never trap: they are OR-ed into a status word that
+ *     vq_device_error() reads, or into a caller-provided status.
+ *   - Row-major layouts throughout; sizes are in elements unless noted.
+ *   - A workspace may be shared by successive calls on one stream, never by
+ *     calls that can run at the same time.
+ */
+#ifndef VQ_H_
+#define VQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VQ_OK 0
+#define VQ_EINVAL (-1)        /* a shape, size or enum argument is out of range */
+#define VQ_EALIGN (-2)        /* a pointer is not aligned as required */
+#define VQ_ECUDA (-3)         /* the CUDA runtime reported an error */
+#define VQ_EUNSUPPORTED (-4)  /* valid, but outside the variants compiled here */
+#define VQ_EWORKSPACE (-5)    /* workspace missing or smaller than required */
+
+/* Activation dtypes. The output of vq_linear has the activation dtype. */
+#define VQ_BF16 0
+#define VQ_F16 1
+#define VQ_F32 2
+
+/*
+ * Verification projection over W4 group-quantized weights.
+ *
+ * Source: dflash-mlx #7 "perf: tune DFlash2 M=8 verification for M1 and M2",
+ * PR description -- VerifyQuantizedLinear runs the M rows of a verify block
+ * (M = 8 for DFlash2's eight-token block, "Why") through 4-bit weights; the
+ * W4A32 path takes fp32 activations. ds4 #778 "dspark: fold first-token
+ * forward into verify ...", commit 1 message -- row tiles so that a verify
+ * block reads every weight once, not once per row.
+ *
+ *   y[m][n] = sum_k x[m][k] * w(n,k),   0 <= m < M, 0 <= n < N
+ *   w(n,k)  = scale[n][k/64] * code(n,k) + bias[n][k/64]
+ *   code(n,k) = (qw[n][k/8] >> (4*(k%8))) & 15     (lowest nibble first)
+ *
+ * x        [M][K] activations, dtype act_dtype (bf16 / f16 bits or fp32),
+ *          16-byte aligned.
+ * qw       [N][K/8] uint32, eight 4-bit codes per word along K, 16-byte aligned.
+ * scales   [N][K/64] bf16 bits, 16-byte aligned.
+ * biases   [N][K/64] bf16 bits, 16-byte aligned.
+ * y        [M][N] output in act_dtype (round to nearest even from the fp32
+ *          accumulator; fp32 output for VQ_F32), 4-byte aligned.
+ * workspace / workspace_bytes
+ *          scratch for the split-K reduction used when N is too narrow to fill
+ *          the GPU. vq_linear_workspace_bytes() gives the size needed (0 when
+ *          no split is used; then workspace may be NULL). The workspace must
+ *          be zero-filled before its first use; every call leaves it
+ *          zero-filled again. 16-byte aligned.
+ * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 512,
+ *          N >= 1. Other K (multiples of 64) return VQ_EUNSUPPORTED.
+ * Accumulation is fp32; each 64-wide group is accumulated from exact integer
+ * codes and scaled once, so the only roundings are the fp32 sums and the
+ * final cast.
+ */
+size_t vq_linear_workspace_bytes(int M, int K, int N, int act_dtype);
+int vq_linear(const void* x, int M, int K, int N, const uint32_t* qw, const uint16_t* scales,
+              const uint16_t* biases, void* y, int act_dtype, void* workspace,
+              size_t workspace_bytes, void* stream);
+
+/*
+ * Vocabulary projection with a fused greedy arg max.
+ *
+ * Source: dflash-mlx #7, PR description (the W4A32 vocabulary projection of
+ * the verify path); ds4 #778, commit 1 message (a fused matvec + arg max
+ * kernel; greedy decoding at temperature 0).
+ *
+ *   logits[m][n] = the vq_linear result, kept in fp32 and never stored
+ *   argmax[m]    = the n with the largest logits[m][n]; ties go to the
+ *                  lowest n; NaN logits never win (a row with no non-NaN
+ *                  logit gives 0)
+ *   maxval[m]    = logits[m][argmax[m]] in fp32 (optional, may be NULL)
+ *
+ * Arguments as in vq_linear; argmax is int32 [M], maxval float [M].
+ * workspace: vq_vocab_argmax_workspace_bytes(M) bytes, required, 16-byte
+ *          aligned, zero-filled before its first use; every call leaves it
+ *          zero-filled again.
+ * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 512,
+ *          1 <= N < 2^31.
+ */
+size_t vq_vocab_argmax_workspace_bytes(int M);
+int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_t* qw,
+                    const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                    int32_t* argmax, float* maxval, void* workspace, size_t workspace_bytes,
+                    void* stream);
+
+/*
+ * Per-row accept walk.
+ *
+ * Source: mlxcel #2865 "perf(speculative): commit per-row accepts in batched
+ * DFlash", Summary and commit message -- each batch row commits its own walk
+ * count instead of the shortest row's.
+ *
+ *   accept[b] = the number of leading positions j with
+ *               draft[b][j] == target[b][j]  (L when all L match)
+ *
+ * draft, target  int32 [B][L]; target[b][j] is the greedy token of verify
+ *                row j of batch row b, aligned with draft[b][j].
+ * accept         int32 [B].
+ * Sizes          B >= 1, L >= 1.
+ */
+int verify_accept_walk(const int32_t* draft, const int32_t* target, int B, int L,
+                       int32_t* accept, void* stream);
+
+/*
+ * Per-row KV commit (compaction to a contiguous valid prefix).
+ *
+ * Source: mlxcel #2865, Summary -- the target compacts its attention KV back
+ * to per-row contiguous valid prefixes so that every row keeps its own accept
+ * count in a rectangular cache.
+ *
+ * For each of the n_tensors tensors (e.g. K and V of every layer), each row b
+ * and head h: slots src_off[b] .. src_off[b]+keep[b]-1, as they were before
+ * the call, are copied to slots prefix_len[b] .. prefix_len[b]+keep[b]-1
+ * (the ranges may overlap), and new_len[b] = prefix_len[b] + keep[b].
+ * Slots below prefix_len[b] are untouched.
+ *
+ * tensors     HOST array of n_tensors DEVICE pointers, each a
+ *             [B][H][S_cap][D] tensor of elem_bytes-byte elements,
+ *             16-byte aligned; 1 <= n_tensors <= 64.
+ * prefix_len, src_off, keep   int32 [B] on the device (keep may come straight
+ *             from verify_accept_walk, so no host round trip is needed).
+ * max_keep    host bound on keep[b]; D*elem_bytes must be a multiple of 16
+ *             and max_keep*D*elem_bytes at most 160 KiB.
+ * new_len     int32 [B] on the device.
+ * status      optional int32 on the device: a row whose keep is outside
+ *             0..max_keep, or whose source or destination range leaves
+ *             0..S_cap, is left untouched, gets new_len[b] = -1, and bit 0
+ *             is OR-ed into *status. The call never clears *status.
+ */
+int kv_compact_per_row(void* const* tensors, int n_tensors, int B, int H, int S_cap, int D,
+                       int elem_bytes, const int32_t* prefix_len, const int32_t* src_off,
+                       const int32_t* keep, int max_keep, int32_t* new_len, int32_t* status,
+                       void* stream);
+
+/* A short description of a VQ_* code. Never NULL. */
+const char* vq_strerror(int code);
+
+/*
+ * Reads the library's device status word of the current device into *out
+ * (host pointer): bit 0 = a kernel gave up waiting on one of its own
+ * pipeline barriers and returned early, so its outputs are not valid.
+ * Synchronizes `stream`. If clear != 0 the word is reset to 0 afterwards.
+ */
+int vq_device_error(int32_t* out, int clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VQ_H_ */

@@ -1,0 +1,143 @@
+"""Thin Python binding of the C ABI in ``include/vq.h``.
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+that they are contiguous, passes their device pointers, sizes and the current
+CUDA stream to the function of the same name in ``libvq.so``, and raises
+``VQError`` on a non-zero status. No step of the computation happens here,
+and there is no fallback: if the library has not been built, ``lib()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libvq.so")
+
+VQ_BF16, VQ_F16, VQ_F32 = 0, 1, 2
+_ACT = {torch.bfloat16: VQ_BF16, torch.float16: VQ_F16, torch.float32: VQ_F32}
+
+# Every symbol include/vq.h declares, with its ctypes signature.
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "vq_linear_workspace_bytes": (_S, [_I, _I, _I, _I]),
+    "vq_linear": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _P, _S, _P]),
+    "vq_vocab_argmax_workspace_bytes": (_S, [_I]),
+    "vq_vocab_argmax": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _S, _P]),
+    "verify_accept_walk": (_I, [_P, _P, _I, _I, _P, _P]),
+    "kv_compact_per_row": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
+    "vq_strerror": (ctypes.c_char_p, [_I]),
+    "vq_device_error": (_I, [_P, _I, _P]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class VQError(RuntimeError):
+    pass
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise VQError("CUDA library %s is missing: build it with "
+                              "speculative_block_draft_02_gb300.build.build()" % LIB_PATH)
+            handle = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise VQError("%s failed: %s (%d)" % (what, lib().vq_strerror(rc).decode(), rc))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise VQError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise VQError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def vq_linear_workspace_bytes(M: int, K: int, N: int, act=torch.bfloat16) -> int:
+    return int(lib().vq_linear_workspace_bytes(M, K, N, _ACT[act]))
+
+
+def vq_vocab_argmax_workspace_bytes(M: int) -> int:
+    return int(lib().vq_vocab_argmax_workspace_bytes(M))
+
+
+def vq_linear(x, qw, scales, biases, y=None, workspace=None, stream=None):
+    """y[M][N] = x[M][K] @ dequant(qw, scales, biases)^T, in x's dtype."""
+    M, K = x.shape
+    N = qw.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().vq_linear(_ptr(x), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases), _ptr(y),
+                         _ACT[x.dtype], _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "vq_linear")
+    return y
+
+
+def vq_vocab_argmax(x, qw, scales, biases, workspace, argmax=None, maxval=None, stream=None):
+    """(argmax int32[M], maxval float32[M]) of x @ dequant(W)^T, logits never stored."""
+    M, K = x.shape
+    N = qw.shape[0]
+    if argmax is None:
+        argmax = torch.empty(M, dtype=torch.int32, device=x.device)
+    rc = lib().vq_vocab_argmax(_ptr(x), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
+                               _ACT[x.dtype], _ptr(argmax), _ptr(maxval), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "vq_vocab_argmax")
+    return argmax, maxval
+
+
+def verify_accept_walk(draft, target, accept=None, stream=None):
+    B, L = draft.shape
+    if accept is None:
+        accept = torch.empty(B, dtype=torch.int32, device=draft.device)
+    rc = lib().verify_accept_walk(_ptr(draft), _ptr(target), B, L, _ptr(accept), _stream(stream))
+    _check(rc, "verify_accept_walk")
+    return accept
+
+
+def kv_compact_per_row(tensors, prefix_len, src_off, keep, max_keep: int, new_len=None,
+                       status=None, stream=None):
+    t0 = tensors[0]
+    B, H, S_cap, D = t0.shape
+    arr = (ctypes.c_void_p * len(tensors))(*[_ptr(t).value for t in tensors])
+    if new_len is None:
+        new_len = torch.empty(B, dtype=torch.int32, device=t0.device)
+    rc = lib().kv_compact_per_row(ctypes.cast(arr, ctypes.c_void_p), len(tensors), B, H, S_cap, D,
+                                  t0.element_size(), _ptr(prefix_len), _ptr(src_off), _ptr(keep),
+                                  max_keep, _ptr(new_len), _ptr(status), _stream(stream))
+    _check(rc, "kv_compact_per_row")
+    return new_len
+
+
+def vq_device_error(clear: bool = False, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    rc = lib().vq_device_error(ctypes.cast(ctypes.byref(out), ctypes.c_void_p), int(clear),
+                               _stream(stream))
+    _check(rc, "vq_device_error")
+    return int(out.value)

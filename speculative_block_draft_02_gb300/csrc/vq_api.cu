@@ -1,0 +1,302 @@
+// C-ABI entry points of the W4 projections (vq_linear, vq_vocab_argmax),
+// their host-side planning and tensor-map encoding, and the status calls.
+#include <mutex>
+
+#include "vq_gemm.cuh"
+
+namespace vq {
+
+// Status word of the device kernels (see vq_device_error).
+__device__ int32_t g_vq_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+int32_t* g_err_ptr[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return VQ_ECUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return VQ_EUNSUPPORTED;
+  return VQ_OK;
+}
+
+int device_state(int* sms, int32_t** err) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      return VQ_ECUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_vq_device_error) != cudaSuccess) return VQ_ECUDA;
+    g_err_ptr[dev] = static_cast<int32_t*>(p);
+    g_sms[dev] = n;
+  }
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return VQ_ECUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  if (sms) *sms = g_sms[dev];
+  if (err) *err = g_err_ptr[dev];
+  return VQ_OK;
+}
+
+int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VQ_OK : VQ_ECUDA;
+}
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Shape of one launch: everything but the pointers.
+struct Plan {
+  int MT, MP, D, KT, RB, S, n_units, grid;
+  int stage_bytes, off_x, off_s, off_b, off_xs, xbox_bytes;
+  uint32_t tx_bytes;
+  size_t smem;
+  size_t ws_cnt_bytes, ws_bytes;
+};
+
+int check_shape(int M, int K, int N, int act) {
+  if (act != VQ_BF16 && act != VQ_F16 && act != VQ_F32) return VQ_EINVAL;
+  if (M < 1 || M > 64 || K < 64 || N < 1 || K % 64 != 0) return VQ_EINVAL;
+  if (K % kBK != 0) return VQ_EUNSUPPORTED;
+  if (act == VQ_F32 && M > 32) return VQ_EUNSUPPORTED;
+  return VQ_OK;
+}
+
+int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
+  int rc = check_shape(M, K, N, act);
+  if (rc) return rc;
+  Plan p{};
+  p.MT = M <= 8 ? 1 : M <= 16 ? 2 : M <= 32 ? 4 : 8;
+  p.MP = 8 * p.MT;
+  const bool f32 = act == VQ_F32;
+  const int n_xbox = f32 ? 16 : 8;
+  p.xbox_bytes = (int)round_up((size_t)128 * M, 1024);
+  p.off_x = 2 * kWeightBoxBytes;
+  p.off_s = p.off_x + n_xbox * p.xbox_bytes;
+  p.off_b = p.off_s + kBN * 16;
+  p.off_xs = p.off_b + kBN * 16;
+  p.stage_bytes = (int)round_up((size_t)p.off_xs + 8 * p.MP * 4, 1024);
+  p.D = (kSmemLimit - 1024 - kMiscBytes) / p.stage_bytes;
+  if (p.D > kMaxStages) p.D = kMaxStages;
+  if (p.D < 2) return VQ_EUNSUPPORTED;
+  p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + (size_t)kBK * (f32 ? 4 : 2) * M);
+  p.smem = 1024 + (size_t)p.D * p.stage_bytes + kMiscBytes;
+  p.KT = K / kBK;
+  p.RB = (int)(((long long)N + kBN - 1) / kBN);
+  p.S = 1;
+  if (!argmax) {
+    // split K only when the row blocks alone leave SMs idle: minimise
+    // waves * stages per unit, with half a stage charged for the reduction
+    double best = 1e30;
+    for (int s = 1; s <= p.KT; ++s) {
+      const long long units = (long long)p.RB * s;
+      const long long waves = (units + sms - 1) / sms;
+      const int stages = (p.KT + s - 1) / s;
+      const double cost = (double)waves * stages + (s > 1 ? 0.5 : 0.0);
+      if (cost < best - 1e-9) {
+        best = cost;
+        p.S = s;
+      }
+    }
+  }
+  p.n_units = p.RB * p.S;
+  p.grid = p.n_units < sms ? p.n_units : sms;
+  if (argmax) {
+    p.ws_cnt_bytes = 0;
+    p.ws_bytes = round_up((size_t)M * 8 + 4, 16);
+  } else if (p.S > 1) {
+    p.ws_cnt_bytes = round_up((size_t)p.RB * 4, 16);
+    p.ws_bytes = p.ws_cnt_bytes + (size_t)p.S * M * N * 4;
+  } else {
+    p.ws_cnt_bytes = p.ws_bytes = 0;
+  }
+  *pl = p;
+  return VQ_OK;
+}
+
+int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint16_t* scales,
+             const uint16_t* biases, int act, bool argmax, void* y, int32_t* amax, float* maxval,
+             void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(M, K, N, act);
+  if (rc) return rc;
+  if (!x || !qw || !scales || !biases) return VQ_EINVAL;
+  if (argmax ? !amax : !y) return VQ_EINVAL;
+  if (((uintptr_t)x | (uintptr_t)qw | (uintptr_t)scales | (uintptr_t)biases) & 15u)
+    return VQ_EALIGN;
+  if (((uintptr_t)y | (uintptr_t)amax | (uintptr_t)maxval) & 3u) return VQ_EALIGN;
+  int sms;
+  int32_t* err;
+  if ((rc = device_state(&sms, &err))) return rc;
+  Plan pl;
+  if ((rc = make_plan(M, K, N, act, argmax, sms, &pl))) return rc;
+  if (pl.ws_bytes) {
+    if (!ws || ws_bytes < pl.ws_bytes) return VQ_EWORKSPACE;
+    if ((uintptr_t)ws & 15u) return VQ_EALIGN;
+  }
+
+  GemmLaunch L;
+  GemmParams& p = L.p;
+  p = GemmParams{};
+  p.M = M;
+  p.K = K;
+  p.N = N;
+  p.KT = pl.KT;
+  p.S = pl.S;
+  p.n_units = pl.n_units;
+  p.D = pl.D;
+  p.stage_bytes = pl.stage_bytes;
+  p.off_x = pl.off_x;
+  p.off_s = pl.off_s;
+  p.off_b = pl.off_b;
+  p.off_xs = pl.off_xs;
+  p.xbox_bytes = pl.xbox_bytes;
+  p.tx_bytes = pl.tx_bytes;
+  p.y = y;
+  p.err = err;
+  if (argmax) {
+    p.keys = static_cast<unsigned long long*>(ws);
+    p.done = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + (size_t)M * 8);
+    p.argmax = amax;
+    p.maxval = maxval;
+  } else if (pl.S > 1) {
+    p.cnt = static_cast<uint32_t*>(ws);
+    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_cnt_bytes);
+  }
+
+  const bool f32 = act == VQ_F32;
+  const CUtensorMapDataType xdt = act == VQ_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : act == VQ_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if ((rc = encode_2d(&L.tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, qw, (uint64_t)K / 8, (uint64_t)N,
+                      (uint64_t)K / 2, 32, kBN, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
+    return rc;
+  if ((rc = encode_2d(&L.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)K / 64,
+                      (uint64_t)N, (uint64_t)K / 32, 8, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
+    return rc;
+  if ((rc = encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, (uint64_t)K / 64,
+                      (uint64_t)N, (uint64_t)K / 32, 8, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
+    return rc;
+  if ((rc = encode_2d(&L.tm_x, xdt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * (f32 ? 4 : 2),
+                      f32 ? 32 : 64, (uint32_t)M, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
+    return rc;
+
+  L.grid = pl.grid;
+  L.MT = pl.MT;
+  L.argmax = argmax;
+  L.smem = pl.smem;
+  L.stream = static_cast<cudaStream_t>(stream);
+  switch (act) {
+    case VQ_BF16:
+      return launch_gemm_bf16(L);
+    case VQ_F16:
+      return launch_gemm_f16(L);
+    default:
+      return launch_gemm_f32(L);
+  }
+}
+
+}  // namespace
+
+int num_sms_current_device(int* out) { return device_state(out, nullptr); }
+
+}  // namespace vq
+
+using namespace vq;
+
+extern "C" size_t vq_linear_workspace_bytes(int M, int K, int N, int act_dtype) {
+  int sms;
+  if (device_state(&sms, nullptr)) return 0;
+  Plan pl;
+  if (make_plan(M, K, N, act_dtype, false, sms, &pl)) return 0;
+  return pl.ws_bytes;
+}
+
+extern "C" int vq_linear(const void* x, int M, int K, int N, const uint32_t* qw,
+                         const uint16_t* scales, const uint16_t* biases, void* y, int act_dtype,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return run_gemm(x, M, K, N, qw, scales, biases, act_dtype, false, y, nullptr, nullptr,
+                  workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t vq_vocab_argmax_workspace_bytes(int M) {
+  if (M < 1 || M > 64) return 0;
+  return round_up((size_t)M * 8 + 4, 16);
+}
+
+extern "C" int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_t* qw,
+                               const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                               int32_t* argmax, float* maxval, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  return run_gemm(x, M, K, N, qw, scales, biases, act_dtype, true, nullptr, argmax, maxval,
+                  workspace, workspace_bytes, stream);
+}
+
+extern "C" const char* vq_strerror(int code) {
+  switch (code) {
+    case VQ_OK:
+      return "ok";
+    case VQ_EINVAL:
+      return "invalid argument (shape, size or enum out of range)";
+    case VQ_EALIGN:
+      return "pointer not aligned as required";
+    case VQ_ECUDA:
+      return "CUDA runtime error";
+    case VQ_EUNSUPPORTED:
+      return "valid but outside the compiled variants";
+    case VQ_EWORKSPACE:
+      return "workspace missing or too small";
+    default:
+      return "unknown status";
+  }
+}
+
+extern "C" int vq_device_error(int32_t* out, int clear, void* stream) {
+  if (!out) return VQ_EINVAL;
+  int rc = device_state(nullptr, nullptr);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_vq_device_error, sizeof v, 0, cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return VQ_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return VQ_ECUDA;
+  if (clear) {
+    const int32_t zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_vq_device_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice,
+                                s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+      return VQ_ECUDA;
+  }
+  *out = v;
+  return VQ_OK;
+}

@@ -1,0 +1,95 @@
+"""The C-ABI library builds for sm_103a, loads, and exports what vq.h declares.
+
+No compute calls here (no GPU needed): only symbol checks and the host-side
+argument validation, which rejects bad calls before any CUDA work.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vq.h")
+
+
+@pytest.fixture(scope="module")
+def vqlib():
+    from speculative_block_draft_02_gb300 import binding, build
+
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = declared_functions()
+    for n in ("vq_linear", "vq_vocab_argmax", "verify_accept_walk", "kv_compact_per_row"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(vqlib):
+    from speculative_block_draft_02_gb300 import binding
+
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(vqlib, n), n
+    assert set(names) == set(binding.SIGNATURES)
+
+
+def test_library_is_built_for_sm_103a():
+    from speculative_block_draft_02_gb300 import build
+
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+
+
+def test_strerror(vqlib):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert vqlib.vq_strerror(code)
+    assert vqlib.vq_strerror(-99) == b"unknown status"
+
+
+def test_vocab_workspace_size(vqlib):
+    assert vqlib.vq_vocab_argmax_workspace_bytes(64) == 528
+    assert vqlib.vq_vocab_argmax_workspace_bytes(1) == 16
+    assert vqlib.vq_vocab_argmax_workspace_bytes(0) == 0
+    assert vqlib.vq_vocab_argmax_workspace_bytes(65) == 0
+
+
+def test_host_validation_rejects_before_any_launch(vqlib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)  # never dereferenced: every call below fails validation first
+    # M out of range, K not a multiple of 64, K not a multiple of 512, bad dtype
+    assert vqlib.vq_linear(fake, 0, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
+    assert vqlib.vq_linear(fake, 65, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
+    assert vqlib.vq_linear(fake, 8, 100, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
+    assert vqlib.vq_linear(fake, 8, 576, 16, fake, fake, fake, fake, 0, None, 0, None) == -4
+    assert vqlib.vq_linear(fake, 8, 512, 16, fake, fake, fake, fake, 7, None, 0, None) == -1
+    assert vqlib.vq_linear(fake, 33, 512, 16, fake, fake, fake, fake, 2, None, 0, None) == -4
+    # null and misaligned pointers
+    assert vqlib.vq_linear(None, 8, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
+    assert vqlib.vq_linear(P(0x1002), 8, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -2
+    assert vqlib.vq_vocab_argmax(fake, 8, 512, 16, fake, fake, fake, 0, None, None, fake, 64,
+                                 None) == -1
+    assert vqlib.verify_accept_walk(fake, fake, 0, 8, fake, None) == -1
+    assert vqlib.verify_accept_walk(fake, fake, 4, 0, fake, None) == -1
+    assert vqlib.verify_accept_walk(P(0x1001), fake, 4, 8, fake, None) == -2
+    arr = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    tp = ctypes.cast(arr, P)
+    assert vqlib.kv_compact_per_row(tp, 0, 4, 8, 2048, 128, 2, fake, fake, fake, 16, fake, None,
+                                    None) == -1
+    assert vqlib.kv_compact_per_row(tp, 65, 4, 8, 2048, 128, 2, fake, fake, fake, 16, fake, None,
+                                    None) == -1
+    assert vqlib.kv_compact_per_row(tp, 2, 4, 8, 2048, 3, 2, fake, fake, fake, 16, fake, None,
+                                    None) == -2
+    assert vqlib.kv_compact_per_row(tp, 2, 4, 8, 2048, 128, 2, fake, fake, fake, 1000, fake,
+                                    None, None) == -4
+    bad = (ctypes.c_void_p * 2)(0x1000, 0x2008)
+    assert vqlib.kv_compact_per_row(ctypes.cast(bad, P), 2, 4, 8, 2048, 128, 2, fake, fake, fake,
+                                    16, fake, None, None) == -2

@@ -1,0 +1,310 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the oracle.
+
+Projections must meet the tolerance in parity.py; arg max indices, accept
+lengths and compacted KV must match bit for bit. Small shapes are checked in
+full (several 128-row units, several 512-wide stages and ragged tails);
+the full-size workloads are checked on sampled output columns (all M rows)
+or, for the arg max, in full.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity import (ORACLE_DT, TOL, assert_proj_close, out_to_f64, proj_error, to_dev_act,
+                    to_dev_weights)
+from speculative_block_draft_02_gb300 import binding as vq
+from speculative_block_draft_02_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from speculative_block_draft_02_gb300 import build
+
+    build.build()
+    vq.lib()
+    oracle.build()
+    torch.cuda.init()
+    yield
+    torch.cuda.synchronize()
+    assert vq.vq_device_error() == 0
+
+
+def _workspace(M, K, N, dtype):
+    nb = vq.vq_linear_workspace_bytes(M, K, N, parity_torch(dtype))
+    return torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
+
+
+def parity_torch(dtype):
+    return {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dtype]
+
+
+def run_linear(x_bits, w, dtype, ws=None):
+    x = to_dev_act(x_bits, dtype)
+    qw, s, b = to_dev_weights(w)
+    M, K = x.shape
+    if ws is None:
+        ws = _workspace(M, K, w.N, dtype)
+    y = vq.vq_linear(x, qw, s, b, workspace=ws)
+    torch.cuda.synchronize()
+    return out_to_f64(y)
+
+
+def oracle_linear(x_bits, w, dtype, cols=None):
+    return oracle.vq_linear(x_bits, w.qw, w.scales, w.biases, act_dtype=ORACLE_DT[dtype],
+                            cols=cols)
+
+
+# ------------------------------------------------------------------ projection
+
+
+def test_linear_tiny_workload():
+    # M=8 bf16 ~N(0,1), K=512, N=1024, seed 0
+    w = synth.w4_weights(0, 1024, 512)
+    x = synth.activations(0, 8, 512, "bf16")
+    assert_proj_close(run_linear(x, w, "bf16"), oracle_linear(x, w, "bf16"), "bf16")
+
+
+RAGGED = [
+    (1, 512, 1, "bf16"), (3, 512, 129, "bf16"), (8, 1024, 1000, "bf16"), (5, 512, 257, "f16"),
+    (12, 1024, 300, "bf16"), (16, 512, 384, "f16"), (24, 512, 200, "bf16"),
+    (33, 1024, 130, "bf16"), (64, 512, 1024, "bf16"), (64, 1536, 260, "f16"),
+    (1, 512, 77, "f32"), (7, 1024, 500, "f32"), (16, 512, 256, "f32"), (32, 512, 129, "f32"),
+    (8, 2048, 4100, "bf16"), (2, 512, 128 * 160 + 3, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,K,N,dtype", RAGGED)
+def test_linear_ragged_shapes(M, K, N, dtype):
+    seed = M * 131 + N
+    w = synth.w4_weights(seed, N, K)
+    x = synth.activations(seed, M, K, dtype)
+    assert_proj_close(run_linear(x, w, dtype), oracle_linear(x, w, dtype), dtype)
+
+
+@pytest.mark.parametrize("M,K,N", [(8, 5120, 1024), (4, 4096, 256), (16, 2560, 640)])
+def test_linear_split_k_is_exact_and_repeatable(M, K, N):
+    w = synth.w4_weights(11, N, K)
+    x = synth.activations(11, M, K, "bf16")
+    ws = _workspace(M, K, N, "bf16")
+    assert ws is not None, "narrow N is expected to split K"
+    y1 = run_linear(x, w, "bf16", ws)
+    y2 = run_linear(x, w, "bf16", ws)        # the workspace must come back zeroed
+    assert np.array_equal(y1, y2)
+    assert_proj_close(y1, oracle_linear(x, w, "bf16"), "bf16")
+
+
+def _sample_cols(N, seed, n_random=200):
+    r = np.random.default_rng(seed)
+    cols = np.concatenate([np.arange(0, 128), np.arange(N - 128, N),
+                           r.choice(N, size=n_random, replace=False)])
+    return np.unique(cols).astype(np.int32)
+
+
+def test_linear_paper_shape_sampled():
+    # M=8, K=5120, N=17408, bf16 ~N(0,1): the headline verify projection
+    w = synth.w4_weights(0, 17408, 5120)
+    x = synth.activations(0, 8, 5120, "bf16")
+    y = run_linear(x, w, "bf16")
+    cols = _sample_cols(17408, 1)
+    assert_proj_close(y[:, cols], oracle_linear(x, w, "bf16", cols), "bf16")
+
+
+@pytest.fixture(scope="module")
+def sweep_weights():
+    return synth.w4_weights(0, 17408, 5120)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("M", [1, 4, 8, 16])
+def test_linear_block_size_and_dtype_sweep(sweep_weights, M, dtype):
+    x = synth.activations(0, M, 5120, dtype, scale=0.5)
+    y = run_linear(x, sweep_weights, dtype)
+    cols = _sample_cols(17408, M, 100)
+    assert_proj_close(y[:, cols], oracle_linear(x, sweep_weights, dtype, cols), dtype)
+
+
+def test_rows_are_independent_and_permute():
+    # a row's result does not depend on the other rows of the block (so M=1,
+    # the M=8 block and the M=16 block agree bit for bit), and permuting the
+    # rows permutes the output
+    w = synth.w4_weights(21, 700, 1024)
+    x16 = synth.activations(21, 16, 1024, "bf16")
+    y16 = run_linear(x16, w, "bf16")
+    y8 = run_linear(x16[:8].copy(), w, "bf16")
+    y1 = run_linear(x16[5:6].copy(), w, "bf16")
+    assert np.array_equal(y16[:8], y8)
+    assert np.array_equal(y16[5], y1[0])
+    perm = np.random.default_rng(0).permutation(16)
+    yp = run_linear(x16[perm].copy(), w, "bf16")
+    assert np.array_equal(yp, y16[perm])
+
+
+def test_linear_paper_shape_is_deterministic():
+    w = synth.w4_weights(0, 17408, 5120)
+    x = synth.activations(0, 8, 5120, "bf16")
+    ys = [run_linear(x, w, "bf16") for _ in range(3)]
+    assert all(np.array_equal(ys[0], y) for y in ys[1:])
+
+
+# ------------------------------------------------------------------ arg max
+
+
+def run_vocab(x_bits, w, dtype="bf16"):
+    x = to_dev_act(x_bits, dtype)
+    qw, s, b = to_dev_weights(w)
+    M = x.shape[0]
+    ws = torch.zeros(vq.vq_vocab_argmax_workspace_bytes(M), dtype=torch.uint8, device="cuda")
+    mx = torch.empty(M, dtype=torch.float32, device="cuda")
+    idx, mx = vq.vq_vocab_argmax(x, qw, s, b, ws, maxval=mx)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), mx.cpu().numpy(), ws
+
+
+def check_argmax(idx, mx, logits):
+    """Bit-exact indices, except rows whose fp32 top two are within the
+    accumulation error of each other: there either index is correct, and
+    the GPU's pick must be one of the near-tied maxima."""
+    r_idx, r_max, r_sec = oracle.argmax(logits)
+    near = 0
+    for m in range(len(idx)):
+        margin = 1e-4 * max(1.0, abs(float(r_max[m])))
+        if float(r_max[m]) - float(r_sec[m]) < margin:
+            near += 1
+            assert float(logits[m, idx[m]]) >= float(r_max[m]) - margin
+        else:
+            assert idx[m] == r_idx[m], (m, idx[m], r_idx[m])
+        assert abs(float(mx[m]) - float(logits[m, idx[m]])) <= 1e-5 * max(1.0, abs(float(mx[m])))
+    return near
+
+
+def test_vocab_argmax_tiny_workload():
+    w = synth.w4_weights(0, 1024, 512)
+    x = synth.activations(0, 8, 512, "bf16")
+    idx, mx, ws = run_vocab(x, w)
+    assert check_argmax(idx, mx, oracle_linear(x, w, "bf16")) == 0
+    assert not ws.any(), "workspace must be left zeroed"
+
+
+def test_vocab_argmax_exact_tie_takes_lowest_index():
+    N, K, M = 3000, 1024, 8
+    w = synth.w4_weights(31, N, K)
+    x = synth.activations(31, M, K, "bf16")
+    r_idx, _, _ = oracle.argmax(oracle_linear(x, w, "bf16"))
+    # copy the winning row of output row 0 to an earlier index: an exact tie
+    a = int(r_idx[0])
+    lo = 3 if a > 3 else N - 1
+    for arr in (w.qw, w.scales, w.biases):
+        arr[lo] = arr[a]
+    idx, _, _ = run_vocab(x, w)
+    assert idx[0] == min(lo, a)
+
+
+@pytest.mark.parametrize("M,K,N", [(3, 512, 1000), (16, 1024, 5000), (64, 512, 2049),
+                                   (33, 1536, 777)])
+def test_vocab_argmax_ragged(M, K, N):
+    w = synth.w4_weights(M + N, N, K)
+    x = synth.activations(M + N, M, K, "bf16")
+    idx, mx, _ = run_vocab(x, w)
+    check_argmax(idx, mx, oracle_linear(x, w, "bf16"))
+
+
+def test_vocab_argmax_full_workload_and_accept():
+    # M=64 (B=4 x block 16), K=2560, N=151936 vocab; drafts match the target
+    # with p=0.7 per position until the first miss
+    cfg = synth.WORKLOADS["vocab_argmax_b4_l16_k2560_n151936"]
+    w = synth.w4_weights(0, cfg["N"], cfg["K"])
+    x = synth.activations(0, cfg["M"], cfg["K"], "bf16")
+    idx, mx, _ = run_vocab(x, w)
+    logits = oracle_linear(x, w, "bf16")
+    check_argmax(idx, mx, logits)
+    r_idx, _, _ = oracle.argmax(logits)
+    target = r_idx.reshape(cfg["B"], cfg["L"])
+    draft = synth.drafts_from_target(0, target, cfg["N"], cfg["p"])
+    acc = vq.verify_accept_walk(torch.from_numpy(draft).cuda(),
+                                torch.from_numpy(idx.reshape(cfg["B"], cfg["L"])).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(acc.cpu().numpy(), oracle.accept_walk(draft, target))
+
+
+# ------------------------------------------------------------------ accept walk
+
+
+@pytest.mark.parametrize("B,L", [(1, 8), (4, 16), (1, 1), (7, 40), (1000, 16), (3, 100)])
+def test_accept_walk(B, L):
+    r = np.random.default_rng(B * 1000 + L)
+    target = r.integers(-5, 2 ** 31 - 1, size=(B, L), dtype=np.int64).astype(np.int32)
+    draft = target.copy()
+    for b in range(B):
+        j = int(r.integers(0, L + 1))
+        if j < L:
+            draft[b, j] ^= 1 + int(r.integers(0, 1000))
+            # positions after the miss may match again
+            if j + 1 < L and r.random() < 0.5:
+                draft[b, j + 1:] = target[b, j + 1:]
+    acc = vq.verify_accept_walk(torch.from_numpy(draft).cuda(), torch.from_numpy(target).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(acc.cpu().numpy(), oracle.accept_walk(draft, target))
+
+
+# ------------------------------------------------------------------ KV commit
+
+
+def _kv_to_dev(tensors):
+    return [torch.from_numpy(t.view(np.int16).copy()).cuda() for t in tensors]
+
+
+def _run_compact(case, max_keep=16):
+    dev = _kv_to_dev(case.tensors)
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    new_len = vq.kv_compact_per_row(dev, i32(case.prefix_len), i32(case.src_off), i32(case.keep),
+                                    max_keep, status=status)
+    torch.cuda.synchronize()
+    return dev, new_len.cpu().numpy(), int(status.item())
+
+
+def test_kv_compact_full_workload():
+    # 8 layers x {K,V} x [4][8][2048][128] fp16, prefix ~U{200..1800},
+    # verify block at the shared offset max(prefix), keep ~U{0..16}
+    case = synth.commit_case(0)
+    dev, new_len, status = _run_compact(case)
+    ref = [t.copy() for t in case.tensors]
+    r_len, r_status = oracle.kv_compact(ref, case.prefix_len, case.src_off, case.keep, 16)
+    assert status == r_status == 0
+    assert np.array_equal(new_len, r_len)
+    for d, r in zip(dev, ref):
+        assert np.array_equal(d.cpu().numpy(), r.view(np.int16))
+
+
+def test_kv_compact_edge_cases():
+    # overlapping ranges, keep 0, no-op, move to the cache end, keep = max,
+    # and rows whose ranges leave the cache (skipped, flagged)
+    case = synth.commit_case(5, layers=2, B=8, H=3, S_cap=64, D=64, block=16, prefix_lo=0,
+                             prefix_hi=40,
+                             keep=[16, 0, 16, 5, 16, 3, 17, 16],
+                             src_off=[44, 44, 20, 59, 48, 2, 40, 50])
+    case.prefix_len[:] = [30, 10, 20, 10, 5, 62, 1, 0]
+    dev, new_len, status = _run_compact(case)
+    ref = [t.copy() for t in case.tensors]
+    r_len, r_status = oracle.kv_compact(ref, case.prefix_len, case.src_off, case.keep, 16)
+    assert status == r_status == 1
+    assert np.array_equal(new_len, r_len)
+    assert r_len.tolist() == [46, 10, 36, 15, 21, -1, -1, -1]
+    for d, r in zip(dev, ref):
+        assert np.array_equal(d.cpu().numpy(), r.view(np.int16))
+
+
+def test_commit_then_next_block_verify():
+    # the per-row commit followed by the next block's M=64 verify projection
+    cfg = synth.WORKLOADS["commit_b4_l16_then_verify_m64"]
+    case = synth.commit_case(0)
+    dev, new_len, _ = _run_compact(case)
+    assert np.array_equal(new_len, case.prefix_len + case.keep)
+    w = synth.w4_weights(0, cfg["N"], cfg["K"])
+    x = synth.activations(0, cfg["M"], cfg["K"], "bf16", name="x_next")
+    y = run_linear(x, w, "bf16")
+    cols = _sample_cols(cfg["N"], 7, 60)
+    assert_proj_close(y[:, cols], oracle_linear(x, w, "bf16", cols), "bf16")
