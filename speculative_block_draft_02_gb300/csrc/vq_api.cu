@@ -102,28 +102,23 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   p.off_b = p.off_s + kBN * 16;
   p.off_xs = p.off_b + kBN * 16;
   p.stage_bytes = (int)round_up((size_t)p.off_xs + 8 * p.MP * 4, 1024);
-  p.D = (kSmemLimit - 1024 - kMiscBytes) / p.stage_bytes;
+  const int red = red_bytes_for(p.MT);
+  p.D = (kSmemLimit - 1024 - kMiscBytes - red) / p.stage_bytes;
   if (p.D > kMaxStages) p.D = kMaxStages;
   if (p.D < 2) return VQ_EUNSUPPORTED;
   p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + (size_t)kBK * (f32 ? 4 : 2) * M);
-  p.smem = 1024 + (size_t)p.D * p.stage_bytes + kMiscBytes;
+  p.smem = 1024 + (size_t)p.D * p.stage_bytes + kMiscBytes + red;
   p.KT = K / kBK;
   p.RB = (int)(((long long)N + kBN - 1) / kBN);
   p.S = 1;
-  if (!argmax) {
-    // split K only when the row blocks alone leave SMs idle: minimise
-    // waves * stages per unit, with half a stage charged for the reduction
-    double best = 1e30;
-    for (int s = 1; s <= p.KT; ++s) {
-      const long long units = (long long)p.RB * s;
-      const long long waves = (units + sms - 1) / sms;
-      const int stages = (p.KT + s - 1) / s;
-      const double cost = (double)waves * stages + (s > 1 ? 0.5 : 0.0);
-      if (cost < best - 1e-9) {
-        best = cost;
-        p.S = s;
-      }
-    }
+  if (!argmax && 2 * p.RB < sms) {
+    // The projection is bound by HBM bandwidth, which half the SMs already
+    // saturate, so K is split only when the row blocks alone would leave
+    // more than half the SMs idle (a narrow N); the split then fills the
+    // SMs in one wave. Each extra slice adds 2*M*N*4 bytes of partials.
+    p.S = sms / p.RB;
+    if (p.S > p.KT) p.S = p.KT;
+    if (p.S < 1) p.S = 1;
   }
   p.n_units = p.RB * p.S;
   p.grid = p.n_units < sms ? p.n_units : sms;

@@ -17,28 +17,37 @@
 // fp32 accumulation; the scale is applied once per group in fp32.
 //
 // Block structure (one CTA per SM, persistent over work units):
-//   warps 0..7  consumers: warp w owns weight rows 16w..16w+15 of the
-//               128-row unit; per 64-wide group it reads its codes from
-//               shared memory, turns nibbles into bf16/f16 integers in
-//               registers and issues mma.sync m16n8k16 with the weights as
-//               the 16-row A operand and the M activation rows as the n8
-//               operand(s), then folds the group into fp32 totals.
-//   warp 8      producer: one lane streams each stage (128 rows x 512 k of
-//               packed codes, their scales and biases, and the matching
-//               x[M][512]) from HBM with cp.async.bulk.tensor (TMA) into a
-//               D-deep ring of shared-memory stages, completion tracked by
-//               mbarriers.
-//   warp 9      helper: computes X_g[m] for the 8 groups of each stage once
-//               per CTA and publishes it to the consumers.
+//   consumers   8*KH warps. Warp w owns weight rows 16*(w%8) .. +15 of the
+//               128-row unit and, when KH = 2, one half of every stage's 8
+//               groups (the two halves are summed at the end of the unit).
+//               Per 64-wide group it reads its codes from shared memory,
+//               turns nibbles into bf16/f16 integers in registers and issues
+//               mma.sync m16n8k16 with the weights as the 16-row A operand
+//               and the M activation rows as the n8 operand(s), then folds
+//               the group into fp32 totals.
+//   producer    one lane streams each stage (128 rows x 512 k of packed
+//               codes, their scales and biases, and the matching x[M][512])
+//               from HBM with cp.async.bulk.tensor (TMA) into a D-deep ring
+//               of shared-memory stages, completion tracked by mbarriers.
+//   helper      one warp computes X_g[m] for the 8 groups of each stage once
+//               per CTA and rewrites the stage's 16-bit x in place into the
+//               MMA's B-fragment order, so consumers load fragments directly.
 // Every weight byte crosses HBM exactly once per call, for all M rows.
+//
+// MMA row i (0..7) of a warp maps to weight row 2i and MMA row i+8 to weight
+// row 2i+1: with the 128-byte TMA swizzle this puts the four rows read by a
+// half-warp on four different bank quarters.
 //
 // Code layout inside a group: thread (g, t) of a warp (g = lane/4,
 // t = lane%4) reads the two 32-bit words 2t, 2t+1 of its rows' 8-word group,
 // i.e. codes k = 16t .. 16t+15. Nibble pair (i, i+4) of a word lands in one
 // bf16x2 register with a single AND/OR against the exponent pattern of
-// 128.0 (bf16) or 1024.0 (f16) followed by an exact subtraction; the MMA's
-// k order within the group is permuted to match, and x is fetched in the
-// same permuted order, so no shuffles of weights are needed.
+// 128.0 (bf16) or 1024.0 (f16), i.e. as the exact integers 128+q / 1024+q;
+// the offset is removed in the fold (bias - 128*scale multiplies X_g). The
+// MMA's k order within the group is permuted to match the pairs, and x is
+// stored in the same permuted order, so no shuffles of weights are needed.
+// fp32 activations (W4A32) are split into three bf16 terms whose sum is x
+// exactly; there the codes are made exact (offset subtracted) before the MMA.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -50,14 +59,20 @@ namespace vq {
 
 constexpr int kBN = 128;             // weight rows per work unit
 constexpr int kBK = 512;             // k per pipeline stage: 8 groups of 64
-constexpr int kConsumerWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kHelperWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kRowTiles = kBN / 16;  // 16-row MMA tiles per unit
 constexpr int kMaxStages = 8;
 constexpr int kWeightBoxBytes = kBN * 128;   // 128 rows x 32 words
-constexpr int kMiscBytes = 256 + 2 * 8 * 64 * 4;
-constexpr int kSmemLimit = 232448;   // 227 KiB opt-in per block
+constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per block
+// misc area after the stage ring: 3 x 8 mbarriers, flags, arg max scratch
+constexpr int kMiscBytes = 256 + 2 * kRowTiles * 64 * 4;
+
+// K-halves per stage (consumer warps = 8 * KH): two for the small-M variants,
+// which are latency-bound, one for the large-M variants, which are bound by
+// MMA issue and need the registers.
+__host__ __device__ constexpr int kh_for(int MT) { return MT <= 2 ? 2 : 1; }
+__host__ __device__ constexpr int threads_for(int MT) { return (kRowTiles * kh_for(MT) + 2) * 32; }
+// bytes of the end-of-unit reduction of the two K-halves
+__host__ __device__ constexpr int red_bytes_for(int MT) { return kh_for(MT) == 2 ? kBN * 8 * MT * 4 : 0; }
 
 struct GemmParams {
   int M, K, N;
@@ -122,27 +137,33 @@ __device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, int3
   }
 }
 
-// Codes (i, i+4) of a word as an exact bf16x2 / f16x2 pair of integers.
-template <bool kF16>
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Codes (i, i+4) of a word as a bf16x2 / f16x2 pair. With kExact the pair is
+// (q_i, q_{i+4}); otherwise it is (M + q_i, M + q_{i+4}) with M = 128 (bf16)
+// or 1024 (f16), one AND/OR and no arithmetic.
+template <bool kF16, bool kExact>
 __device__ __forceinline__ uint32_t code_pair(uint32_t word, int i) {
   constexpr uint32_t kMagic = kF16 ? 0x64006400u : 0x43004300u;   // 1024.0 / 128.0
   const uint32_t v = lop3_and_or(word >> (4 * i), 0x000F000Fu, kMagic);
-  uint32_t r;
-  if constexpr (kF16) {
+  if constexpr (!kExact) {
+    return v;
+  } else if constexpr (kF16) {
     const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v),
                               *reinterpret_cast<const __half2*>(&kMagic));
-    r = *reinterpret_cast<const uint32_t*>(&h);
+    return *reinterpret_cast<const uint32_t*>(&h);
   } else {
     const __nv_bfloat162 h = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&v),
                                      *reinterpret_cast<const __nv_bfloat162*>(&kMagic));
-    r = *reinterpret_cast<const uint32_t*>(&h);
+    return *reinterpret_cast<const uint32_t*>(&h);
   }
-  return r;
 }
 
-// Element j (0..7) of eight packed bf16 values, widened exactly to fp32.
-__device__ __forceinline__ float bf16_at(const uint4& v, int j) {
-  const uint32_t w = (j >> 1) == 0 ? v.x : (j >> 1) == 1 ? v.y : (j >> 1) == 2 ? v.z : v.w;
+// Element j (0..3) of four packed bf16 values, widened exactly to fp32.
+__device__ __forceinline__ float bf16_at(const uint2& v, int j) {
+  const uint32_t w = (j >> 1) ? v.y : v.x;
   return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
@@ -188,27 +209,33 @@ __device__ __forceinline__ bool better(float v, uint32_t n, bool has, float bv, 
   return v > bv || (v == bv && n < bn);
 }
 
-// One 512-wide stage for this thread's rows lr, lr+8: totals += sum over the
-// stage's 8 groups of scale*A_g + bias*X_g.
+// Four groups (4kh .. 4kh+3) of one 512-wide stage for this thread's weight
+// rows r0, r0+1: totals += scale * A_g + bias * X_g per group.
 template <int ACT, int MT>
-__device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParams& p, int lr,
-                                              int g, int t, float (&tot)[MT][4]) {
+__device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParams& p, int rt,
+                                              int kh, int g, int t, float (&tot)[MT][4]) {
   constexpr bool kF16 = (ACT == VQ_F16);
+  constexpr bool kF32 = (ACT == VQ_F32);
   constexpr int MP = 8 * MT;
-  const uint4 sv0 = *reinterpret_cast<const uint4*>(st + p.off_s + lr * 16);
-  const uint4 sv1 = *reinterpret_cast<const uint4*>(st + p.off_s + (lr + 8) * 16);
-  const uint4 bv0 = *reinterpret_cast<const uint4*>(st + p.off_b + lr * 16);
-  const uint4 bv1 = *reinterpret_cast<const uint4*>(st + p.off_b + (lr + 8) * 16);
+  // codes enter the MMA as (offset + q) except for fp32 activations
+  constexpr float kOffset = kF32 ? 0.f : (kF16 ? 1024.f : 128.f);
+  const int r0 = 16 * rt + 2 * g;   // weight rows r0 (MMA row g) and r0+1 (MMA row g+8)
+  const uint2 sv0 = *reinterpret_cast<const uint2*>(st + p.off_s + r0 * 16 + kh * 8);
+  const uint2 sv1 = *reinterpret_cast<const uint2*>(st + p.off_s + (r0 + 1) * 16 + kh * 8);
+  const uint2 bv0 = *reinterpret_cast<const uint2*>(st + p.off_b + r0 * 16 + kh * 8);
+  const uint2 bv1 = *reinterpret_cast<const uint2*>(st + p.off_b + (r0 + 1) * 16 + kh * 8);
   const float* xs = reinterpret_cast<const float*>(st + p.off_xs);
+  const uint8_t* wbox = st + kh * kWeightBoxBytes;   // groups 4kh .. 4kh+3
+  const int sw0 = r0 & 7, sw1 = (r0 + 1) & 7;        // 128-byte swizzle of the two rows
 
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    // codes: 128-byte rows, 16-byte chunks swizzled by (row % 8) == g
-    const uint8_t* wbox = st + (j >> 2) * kWeightBoxBytes;
-    const int inoff = (((2 * (j & 3) + (t >> 1)) ^ g) << 4) + ((t & 1) << 3);
-    const uint2 wa = *reinterpret_cast<const uint2*>(wbox + lr * 128 + inoff);
-    const uint2 wb = *reinterpret_cast<const uint2*>(wbox + (lr + 8) * 128 + inoff);
-
+  for (int jj = 0; jj < 4; ++jj) {
+    const int j = 4 * kh + jj;
+    const int cw = 2 * jj + (t >> 1);                 // 16-byte chunk of words 2t, 2t+1
+    const uint2 wa = *reinterpret_cast<const uint2*>(wbox + r0 * 128 + ((cw ^ sw0) << 4) +
+                                                     ((t & 1) << 3));
+    const uint2 wb = *reinterpret_cast<const uint2*>(wbox + (r0 + 1) * 128 + ((cw ^ sw1) << 4) +
+                                                     ((t & 1) << 3));
     float acc[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
@@ -217,8 +244,9 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParam
     for (int h = 0; h < 2; ++h) {
       const uint32_t qa = h ? wa.y : wa.x;
       const uint32_t qb = h ? wb.y : wb.x;
-      if constexpr (ACT != VQ_F32) {
-        // x[m][64j + 16t + 8h + 0..7], one 16-byte chunk of line m
+      if constexpr (!kF32) {
+        // x[m][64j + 16t + 8h + i], stored by the helper as the fragment
+        // pairs (x0,x4) (x1,x5) (x2,x6) (x3,x7)
         uint4 xv[MT];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
@@ -231,16 +259,13 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParam
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
           uint32_t a[4];
-          a[0] = code_pair<kF16>(qa, 2 * s2);
-          a[1] = code_pair<kF16>(qb, 2 * s2);
-          a[2] = code_pair<kF16>(qa, 2 * s2 + 1);
-          a[3] = code_pair<kF16>(qb, 2 * s2 + 1);
+          a[0] = code_pair<kF16, false>(qa, 2 * s2);
+          a[1] = code_pair<kF16, false>(qb, 2 * s2);
+          a[2] = code_pair<kF16, false>(qa, 2 * s2 + 1);
+          a[3] = code_pair<kF16, false>(qb, 2 * s2 + 1);
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const uint32_t lo = s2 ? xv[mt].y : xv[mt].x;
-            const uint32_t hi = s2 ? xv[mt].w : xv[mt].z;
-            mma_16816<kF16>(acc[mt], a, prmt(lo, hi, 0x5410u), prmt(lo, hi, 0x7632u));
-          }
+          for (int mt = 0; mt < MT; ++mt)
+            mma_16816<kF16>(acc[mt], a, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
         }
       } else {
         // fp32 x: half-group boxes of 32 values; this thread's 8 values are
@@ -260,10 +285,10 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParam
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
           uint32_t a[4];
-          a[0] = code_pair<false>(qa, 2 * s2);
-          a[1] = code_pair<false>(qb, 2 * s2);
-          a[2] = code_pair<false>(qa, 2 * s2 + 1);
-          a[3] = code_pair<false>(qb, 2 * s2 + 1);
+          a[0] = code_pair<false, true>(qa, 2 * s2);
+          a[1] = code_pair<false, true>(qb, 2 * s2);
+          a[2] = code_pair<false, true>(qa, 2 * s2 + 1);
+          a[3] = code_pair<false, true>(qb, 2 * s2 + 1);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
             const float e0 = s2 ? x0[mt].z : x0[mt].x;   // x_{2s'}
@@ -281,9 +306,11 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParam
       }
     }
 
-    // fold group j: scale the exact-code sums, add bias * sum(x)
-    const float s_a = bf16_at(sv0, j), s_b = bf16_at(sv1, j);
-    const float c_a = bf16_at(bv0, j), c_b = bf16_at(bv1, j);
+    // fold group j: scale the code sums; the bias term (less the code
+    // offset) multiplies the group sum of x
+    const float s_a = bf16_at(sv0, jj), s_b = bf16_at(sv1, jj);
+    const float c_a = fmaf(-kOffset, s_a, bf16_at(bv0, jj));
+    const float c_b = fmaf(-kOffset, s_b, bf16_at(bv1, jj));
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       const float2 xsum = *reinterpret_cast<const float2*>(xs + j * MP + 8 * mt + 2 * t);
@@ -295,53 +322,72 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParam
   }
 }
 
-// Sum over the 64 values of group j, row m, of one stage's x (any dtype).
-template <int ACT>
-__device__ __forceinline__ float group_sum(const uint8_t* st, const GemmParams& p, int j, int m) {
-  float s = 0.f;
-  if constexpr (ACT == VQ_F32) {
+// Helper work on one landed stage: X_g[m] for every group and row, and (for
+// 16-bit x) each 16-byte chunk of x rewritten in place as the fragment pairs
+// (x0,x4) (x1,x5) (x2,x6) (x3,x7).
+template <int ACT, int MT>
+__device__ __forceinline__ void prepare_stage(uint8_t* st, const GemmParams& p, int lane) {
+  constexpr int MP = 8 * MT;
+  float* xs = reinterpret_cast<float*>(st + p.off_xs);
+  for (int idx = lane; idx < 8 * MP; idx += 32) {
+    const int j = idx / MP, m = idx - (idx / MP) * MP;
+    float s = 0.f;
+    if (m < p.M) {
+      if constexpr (ACT == VQ_F32) {
 #pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-      const uint8_t* line = st + p.off_x + (2 * j + hb) * p.xbox_bytes + m * 128;
+        for (int hb = 0; hb < 2; ++hb) {
+          const uint8_t* line = st + p.off_x + (2 * j + hb) * p.xbox_bytes + m * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(line + ((c ^ (m & 7)) << 4));
-        s += v.x;
-        s += v.y;
-        s += v.z;
-        s += v.w;
-      }
-    }
-  } else {
-    const uint8_t* line = st + p.off_x + j * p.xbox_bytes + m * 128;
+          for (int c = 0; c < 8; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(line + ((c ^ (m & 7)) << 4));
+            s += v.x;
+            s += v.y;
+            s += v.z;
+            s += v.w;
+          }
+        }
+      } else {
+        uint8_t* line = st + p.off_x + j * p.xbox_bytes + m * 128;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(line + ((c ^ (m & 7)) << 4));
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        for (int c = 0; c < 8; ++c) {
+          uint4* ptr = reinterpret_cast<uint4*>(line + ((c ^ (m & 7)) << 4));
+          const uint4 v = *ptr;
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if constexpr (ACT == VQ_F16) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-          s += f.x;
-          s += f.y;
-        } else {
-          s += __uint_as_float(w[e] << 16);
-          s += __uint_as_float(w[e] & 0xFFFF0000u);
+          for (int e = 0; e < 4; ++e) {
+            if constexpr (ACT == VQ_F16) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+              s += f.x;
+              s += f.y;
+            } else {
+              s += __uint_as_float(w[e] << 16);
+              s += __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+          }
+          *ptr = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
+                            prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
         }
       }
     }
+    xs[idx] = s;
   }
-  return s;
+  // the slot is refilled by TMA (async proxy) after these generic writes
+  fence_proxy_async_smem();
 }
 
 template <int ACT, int MT, bool ARGMAX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(MT), 1)
     vq_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_x,
                    const GemmParams p) {
   constexpr int MP = 8 * MT;
+  constexpr int KH = kh_for(MT);
+  constexpr int kConsumers = kRowTiles * KH;          // consumer warps
+  constexpr int kProducerWarp = kConsumers;
+  constexpr int kHelperWarp = kConsumers + 1;
   constexpr int kXBoxes = (ACT == VQ_F32) ? 16 : 8;
   constexpr int kXBoxElems = kBK / kXBoxes;
+  constexpr uint32_t kEpiThreads = kRowTiles * 32;     // the K-half-0 consumers
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -352,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 192);
   volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 196);
   float* const red_v = reinterpret_cast<float*>(misc + 256);
-  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + 8 * 64 * 4);
+  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + kRowTiles * 64 * 4);
+  float* const red_k = reinterpret_cast<float*>(misc + kMiscBytes);   // K-half partials
   auto full_bar = [&](int s) { return misc_a + 8u * s; };
   auto empty_bar = [&](int s) { return misc_a + 64u + 8u * s; };
   auto xsum_bar = [&](int s) { return misc_a + 128u + 8u * s; };
@@ -361,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.D; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumerWarps + 1);
+      mbar_init(empty_bar(s), kConsumers + 1);
       mbar_init(xsum_bar(s), 32);
     }
     *abort_flag = 0;
@@ -411,23 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp == kHelperWarp) {
-    // ------------------------------------------------------------ helper: X_g[m]
+    // ------------------------------------------------------------ helper
     int q = 0;
     for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-      const int rb = u / p.S, sp = u - rb * p.S;
-      (void)rb;
+      const int sp = u - (u / p.S) * p.S;
       const int kt0 = sp * p.KT / p.S, kt1 = (sp + 1) * p.KT / p.S;
       for (int kt = kt0; kt < kt1; ++kt, ++q) {
         const int slot = q % p.D;
         const uint32_t ph = (uint32_t)(q / p.D) & 1u;
-        if (wait_or_abort(full_bar(slot), ph, abort_flag, p.err)) {
-          uint8_t* st = sbase + slot * p.stage_bytes;
-          float* xs = reinterpret_cast<float*>(st + p.off_xs);
-          for (int idx = lane; idx < 8 * MP; idx += 32) {
-            const int j = idx / MP, m = idx - (idx / MP) * MP;
-            xs[idx] = (m < p.M) ? group_sum<ACT>(st, p, j, m) : 0.f;
-          }
-        }
+        if (wait_or_abort(full_bar(slot), ph, abort_flag, p.err))
+          prepare_stage<ACT, MT>(sbase + slot * p.stage_bytes, p, lane);
         mbar_arrive(xsum_bar(slot));
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(slot));
@@ -438,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
-  const int lr = 16 * warp + g;
+  const int rt = warp % kRowTiles, kh = warp / kRowTiles;
+  const int r0 = 16 * rt + 2 * g;
   float best_v[MT][2];
   uint32_t best_n[MT][2];
   bool best_has[MT][2];
@@ -466,7 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = !aborted && wait_or_abort(full_bar(slot), ph, abort_flag, p.err) &&
                       wait_or_abort(xsum_bar(slot), ph, abort_flag, p.err);
       if (ok) {
-        consume_stage<ACT, MT>(sbase + slot * p.stage_bytes, p, lr, g, t, tot);
+        consume_stage<ACT, MT>(sbase + slot * p.stage_bytes, p, rt, kh, g, t, tot);
+        if constexpr (KH == 1)   // one warp per row tile covers both halves
+          consume_stage<ACT, MT>(sbase + slot * p.stage_bytes, p, rt, 1, g, t, tot);
       } else {
         aborted = true;
       }
@@ -474,7 +517,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(empty_bar(slot));
     }
 
-    const int n0 = rb * kBN + lr;
+    if constexpr (KH == 2) {
+      // add the second K-half into the first; red_k is [128 rows][MP]
+      if (kh == 1) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            red_k[(r0 + (e >> 1)) * MP + 8 * mt + 2 * t + (e & 1)] = tot[mt][e];
+      }
+      named_bar_sync(1, kConsumers * 32);
+      if (kh == 0) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            tot[mt][e] += red_k[(r0 + (e >> 1)) * MP + 8 * mt + 2 * t + (e & 1)];
+      }
+      named_bar_sync(1, kConsumers * 32);
+      if (kh == 1) continue;
+    }
+
+    const int n0 = rb * kBN + r0;   // this thread's rows n0 (e < 2) and n0 + 1
     if constexpr (!ARGMAX) {
       if (p.S == 1) {
         if (!aborted) {
@@ -482,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int n = n0 + (e >> 1) * 8, m = 8 * mt + 2 * t + (e & 1);
+              const int n = n0 + (e >> 1), m = 8 * mt + 2 * t + (e & 1);
               if (n < p.N && m < p.M) store_out<ACT>(p.y, (size_t)m * p.N + n, tot[mt][e]);
             }
         }
@@ -495,14 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int n = n0 + (e >> 1) * 8, m = 8 * mt + 2 * t + (e & 1);
+              const int n = n0 + (e >> 1), m = 8 * mt + 2 * t + (e & 1);
               if (n < p.N && m < p.M) __stcg(part + (size_t)m * p.N + n, tot[mt][e]);
             }
         }
         __threadfence();
-        named_bar_sync(1, kConsumerWarps * 32);
+        named_bar_sync(2, kEpiThreads);
         if (threadIdx.x == 0) *epi_flag = (atomicAdd(p.cnt + rb, 1u) == (uint32_t)(p.S - 1));
-        named_bar_sync(1, kConsumerWarps * 32);
+        named_bar_sync(2, kEpiThreads);
         if (*epi_flag) {
           __threadfence();
           if (!aborted) {
@@ -510,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const int n = n0 + (e >> 1) * 8, m = 8 * mt + 2 * t + (e & 1);
+                const int n = n0 + (e >> 1), m = 8 * mt + 2 * t + (e & 1);
                 if (n < p.N && m < p.M) {
                   float s = 0.f;
                   for (int k = 0; k < p.S; ++k)
@@ -521,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (threadIdx.x == 0) p.cnt[rb] = 0u;
         }
+        named_bar_sync(2, kEpiThreads);
       }
     } else {
       // running arg max per output row m over this thread's columns n
@@ -529,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int n = n0 + (e >> 1) * 8, c = e & 1;
+          const int n = n0 + (e >> 1), c = e & 1;
           const float v = tot[mt][e] + 0.0f;   // -0 -> +0
           if (!aborted && n < p.N && !(v != v)) {
             if (!best_has[mt][c] || v > best_v[mt][c]) {
@@ -543,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if constexpr (ARGMAX) {
-    // reduce over the 8 row-lanes g of the warp, then over the 8 warps
+    if (KH == 2 && kh == 1) return;
+    // reduce over the 8 row-lanes g of the warp, then over the 8 row tiles
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -564,17 +630,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (g == 0) {
           const int m = 8 * mt + 2 * t + c;
-          red_v[warp * 64 + m] = v;
-          red_i[warp * 64 + m] = h ? n : 0xFFFFFFFFu;
+          red_v[rt * 64 + m] = v;
+          red_i[rt * 64 + m] = h ? n : 0xFFFFFFFFu;
         }
       }
-    named_bar_sync(1, kConsumerWarps * 32);
+    named_bar_sync(2, kEpiThreads);
     if (threadIdx.x < MP) {
       const int m = threadIdx.x;
       float v = 0.f;
       uint32_t n = 0u;
       bool h = false;
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < kRowTiles; ++w) {
         const uint32_t on = red_i[w * 64 + m];
         const float ov = red_v[w * 64 + m];
         if (better(ov, on, on != 0xFFFFFFFFu, v, n, h)) {
@@ -590,9 +656,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __threadfence();
-    named_bar_sync(1, kConsumerWarps * 32);
+    named_bar_sync(2, kEpiThreads);
     if (threadIdx.x == 0) *epi_flag = (atomicAdd(p.done, 1u) == gridDim.x - 1);
-    named_bar_sync(1, kConsumerWarps * 32);
+    named_bar_sync(2, kEpiThreads);
     if (*epi_flag) {
       __threadfence();
       if (threadIdx.x < p.M) {
@@ -617,7 +683,7 @@ int launch_one(const GemmLaunch& L) {
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem) !=
       cudaSuccess)
     return VQ_ECUDA;
-  k<<<L.grid, kThreads, L.smem, L.stream>>>(L.tm_w, L.tm_s, L.tm_b, L.tm_x, L.p);
+  k<<<L.grid, threads_for(MT), L.smem, L.stream>>>(L.tm_w, L.tm_s, L.tm_b, L.tm_x, L.p);
   return cudaGetLastError() == cudaSuccess ? VQ_OK : VQ_ECUDA;
 }
 
