@@ -69,12 +69,43 @@ int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t 
   return r == CUDA_SUCCESS ? VQ_OK : VQ_ECUDA;
 }
 
+// x viewed as [K/inner][M][inner] (group-major), so one box brings a stage's
+// x for all M rows as [group][row][128 bytes]. The strides are not
+// increasing; if the driver rejects that view the caller falls back to one
+// 2-D box per group.
+int encode_x3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int M, int K,
+               int elem_bytes, int box_rows, int box_groups) {
+  const uint64_t inner = 128 / elem_bytes;
+  const cuuint64_t dims[3] = {inner, (cuuint64_t)M, (cuuint64_t)K / inner};
+  const cuuint64_t strides[2] = {(cuuint64_t)K * elem_bytes, 128};
+  const cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)box_rows, (cuuint32_t)box_groups};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VQ_OK : VQ_ECUDA;
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int red_bytes(int MT) {
+  switch (MT) {
+    case 1:
+      return Cfg<1>::RED;
+    case 2:
+      return Cfg<2>::RED;
+    case 4:
+      return Cfg<4>::RED;
+    default:
+      return Cfg<8>::RED;
+  }
+}
 
 // Shape of one launch: everything but the pointers.
 struct Plan {
   int MT, MP, D, KT, RB, S, n_units, grid;
-  int stage_bytes, off_x, off_s, off_b, off_xs, xbox_bytes;
+  int stage_bytes, off_x, off_s, off_b, xbox_bytes, xt, tab_bytes;
   uint32_t tx_bytes;
   size_t smem;
   size_t ws_cnt_bytes, ws_bytes;
@@ -96,18 +127,39 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   p.MP = 8 * p.MT;
   const bool f32 = act == VQ_F32;
   const int n_xbox = f32 ? 16 : 8;
-  p.xbox_bytes = (int)round_up((size_t)128 * M, 1024);
-  p.off_x = 2 * kWeightBoxBytes;
-  p.off_s = p.off_x + n_xbox * p.xbox_bytes;
-  p.off_b = p.off_s + kBN * 16;
-  p.off_xs = p.off_b + kBN * 16;
-  p.stage_bytes = (int)round_up((size_t)p.off_xs + 8 * p.MP * 4, 1024);
-  const int red = red_bytes_for(p.MT);
-  p.D = (kSmemLimit - 1024 - kMiscBytes - red) / p.stage_bytes;
+  // x for the stage: [group][8*MT rows][128 B]; rows >= M are zero-filled.
+  // For 16-bit x with M <= 8 whose fp16 table fits, x is converted once per
+  // block instead (the x-table variant) and the stages carry weights only.
+  const int red = red_bytes(p.MT);
+  // (the conversion costs about as much as two row blocks of the main loop
+  // save, so it is used only when a block processes several row blocks)
+  const long long rb_total = ((long long)N + kBN - 1) / kBN;
+  const long long per_block = argmax ? (rb_total + sms - 1) / sms : (rb_total >= sms ? (rb_total + sms - 1) / sms : 1);
+  p.xt = (!f32 && p.MT == 1 && xt_table_bytes(K) <= kMaxXtBytes && per_block >= 3) ? 1 : 0;
+  int tab;
+  if (p.xt) {
+    p.xbox_bytes = 0;
+    p.off_x = 0;
+    p.off_s = xt_stage_off_s();
+    p.off_b = xt_stage_off_s() + kBN * 16;
+    p.stage_bytes = xt_stage_bytes();
+    tab = xt_table_bytes(K);
+  } else {
+    p.xbox_bytes = 128 * p.MP;
+    p.off_x = stage_off_x();
+    p.off_s = stage_off_s(act, p.MT);
+    p.off_b = stage_off_b(act, p.MT);
+    p.stage_bytes = stage_bytes(act, p.MT);
+    tab = xsum_bytes(K, p.MT);
+    if (tab > kMaxXsumBytes) return VQ_EUNSUPPORTED;
+  }
+  tab = (int)round_up((size_t)tab, 1024);
+  p.D = (kSmemLimit - 1024 - kMiscBytes - red - tab) / p.stage_bytes;
   if (p.D > kMaxStages) p.D = kMaxStages;
   if (p.D < 2) return VQ_EUNSUPPORTED;
-  p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + (size_t)kBK * (f32 ? 4 : 2) * M);
-  p.smem = 1024 + (size_t)p.D * p.stage_bytes + kMiscBytes + red;
+  p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + (size_t)n_xbox * p.xbox_bytes);
+  p.tab_bytes = tab;
+  p.smem = 1024 + (size_t)p.D * p.stage_bytes + kMiscBytes + red + tab;
   p.KT = K / kBK;
   p.RB = (int)(((long long)N + kBN - 1) / kBN);
   p.S = 1;
@@ -158,6 +210,7 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
   GemmLaunch L;
   GemmParams& p = L.p;
   p = GemmParams{};
+  p.x = x;
   p.M = M;
   p.K = K;
   p.N = N;
@@ -169,9 +222,10 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
   p.off_x = pl.off_x;
   p.off_s = pl.off_s;
   p.off_b = pl.off_b;
-  p.off_xs = pl.off_xs;
-  p.xbox_bytes = pl.xbox_bytes;
+
   p.tx_bytes = pl.tx_bytes;
+  p.xt = pl.xt;
+  p.tab_bytes = pl.tab_bytes;
   p.y = y;
   p.err = err;
   if (argmax) {
@@ -200,10 +254,18 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
                       (uint64_t)N, (uint64_t)K / 32, 8, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
     return rc;
-  if ((rc = encode_2d(&L.tm_x, xdt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * (f32 ? 4 : 2),
-                      f32 ? 32 : 64, (uint32_t)M, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
-    return rc;
+  const int eb = f32 ? 4 : 2;
+  // box rows = 8*MT >= M: the rows past M are out of range and arrive zeroed;
+  // the x-table variant takes every group of K in one box
+  if (encode_x3d(&L.tm_x, xdt, x, M, K, eb, pl.MP, pl.xt ? K / 64 : kBK / (128 / eb)) == VQ_OK) {
+    p.x3d = 1;
+  } else {
+    if ((rc = encode_2d(&L.tm_x, xdt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * eb, 128 / eb,
+                        (uint32_t)pl.MP, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
+      return rc;
+    p.x3d = 0;
+  }
 
   L.grid = pl.grid;
   L.MT = pl.MT;

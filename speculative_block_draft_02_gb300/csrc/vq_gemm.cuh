@@ -17,21 +17,23 @@
 // fp32 accumulation; the scale is applied once per group in fp32.
 //
 // Block structure (one CTA per SM, persistent over work units):
-//   consumers   8*KH warps. Warp w owns weight rows 16*(w%8) .. +15 of the
-//               128-row unit and, when KH = 2, one half of every stage's 8
-//               groups (the two halves are summed at the end of the unit).
-//               Per 64-wide group it reads its codes from shared memory,
-//               turns nibbles into bf16/f16 integers in registers and issues
-//               mma.sync m16n8k16 with the weights as the 16-row A operand
-//               and the M activation rows as the n8 operand(s), then folds
-//               the group into fp32 totals.
+//   consumers   TEAMS teams of warps; team i takes the stages q with
+//               q % TEAMS == i, so one team's stage boundary overlaps the
+//               other team's work. Within a team each warp owns RT 16-row MMA
+//               tiles of the 128-row unit and a K-slice of GPW groups of its
+//               stages (all partial sums of a row tile are added at the end
+//               of the unit). Per 64-wide group a warp reads its codes from
+//               shared memory, turns nibbles into bf16/f16 integers in
+//               registers and issues mma.sync m16n8k16 with the weights as
+//               the 16-row A operand and the M activation rows as the n8
+//               operand(s), then folds the group into fp32 totals.
+//               X_g[m] for every group of K is computed once per block from
+//               global x while the first stages are in flight, and kept in
+//               shared memory.
 //   producer    one lane streams each stage (128 rows x 512 k of packed
 //               codes, their scales and biases, and the matching x[M][512])
 //               from HBM with cp.async.bulk.tensor (TMA) into a D-deep ring
 //               of shared-memory stages, completion tracked by mbarriers.
-//   helper      one warp computes X_g[m] for the 8 groups of each stage once
-//               per CTA and rewrites the stage's 16-bit x in place into the
-//               MMA's B-fragment order, so consumers load fragments directly.
 // Every weight byte crosses HBM exactly once per call, for all M rows.
 //
 // MMA row i (0..7) of a warp maps to weight row 2i and MMA row i+8 to weight
@@ -44,8 +46,9 @@
 // bf16x2 register with a single AND/OR against the exponent pattern of
 // 128.0 (bf16) or 1024.0 (f16), i.e. as the exact integers 128+q / 1024+q;
 // the offset is removed in the fold (bias - 128*scale multiplies X_g). The
-// MMA's k order within the group is permuted to match the pairs, and x is
-// stored in the same permuted order, so no shuffles of weights are needed.
+// MMA's k order within the group is permuted to match the pairs, and the x
+// fragments are permuted the same way with byte permutes, so the weights are
+// never shuffled.
 // fp32 activations (W4A32) are split into three bf16 terms whose sum is x
 // exactly; there the codes are made exact (offset subtracted) before the MMA.
 #pragma once
@@ -59,30 +62,74 @@ namespace vq {
 
 constexpr int kBN = 128;             // weight rows per work unit
 constexpr int kBK = 512;             // k per pipeline stage: 8 groups of 64
-constexpr int kRowTiles = kBN / 16;  // 16-row MMA tiles per unit
 constexpr int kMaxStages = 8;
 constexpr int kWeightBoxBytes = kBN * 128;   // 128 rows x 32 words
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per block
-// misc area after the stage ring: 3 x 8 mbarriers, flags, arg max scratch
-constexpr int kMiscBytes = 256 + 2 * kRowTiles * 64 * 4;
+// misc area after the stage ring: 2 x 8 mbarriers, flags, arg max scratch
+constexpr int kMiscBytes = 256 + 2 * 8 * 64 * 4;
 
-// K-halves per stage (consumer warps = 8 * KH): two for the small-M variants,
-// which are latency-bound, one for the large-M variants, which are bound by
-// MMA issue and need the registers.
-__host__ __device__ constexpr int kh_for(int MT) { return MT <= 2 ? 2 : 1; }
-__host__ __device__ constexpr int threads_for(int MT) { return (kRowTiles * kh_for(MT) + 2) * 32; }
-// bytes of the end-of-unit reduction of the two K-halves
-__host__ __device__ constexpr int red_bytes_for(int MT) { return kh_for(MT) == 2 ? kBN * 8 * MT * 4 : 0; }
+// Work split of the consumers by the number MT of n8 tiles (M <= 8*MT):
+// TEAMS teams taking alternate stages, RT 16-row tiles per warp (two tiles
+// share the x fragments), KQ K-slices per stage within a team, GPW = 8/KQ
+// groups per warp and stage.
+template <int MT>
+struct Cfg {
+  static constexpr int TEAMS = MT <= 2 ? 2 : 1;   // a power of two
+  static constexpr int RT = MT <= 2 ? 2 : 1;
+  static constexpr int KQ = MT <= 2 ? 2 : 1;
+  static constexpr int GPW = 8 / KQ;
+  static constexpr int RW = 8 / RT;                 // warps along the rows
+  static constexpr int WPT = RW * KQ;               // warps per team
+  static constexpr int WARPS = WPT * TEAMS;         // consumer warps
+  static constexpr int THREADS = (WARPS + 1) * 32;  // + the producer warp
+  static constexpr int SLICES = TEAMS * KQ;         // partial sums per row
+  static constexpr int RED = (SLICES - 1) * kBN * 8 * MT * 4;
+};
+
+// Stage layout in shared memory (bytes from the 1 KiB-aligned stage start):
+// codes [2][128 rows][128 B] (two 128-byte TMA boxes, 128-byte swizzle),
+// x [groups][8*MT rows][128 B] (swizzled), scales [128][16 B], biases [128][16 B].
+__host__ __device__ constexpr int x_boxes(int act) { return act == VQ_F32 ? 16 : 8; }
+__host__ __device__ constexpr int stage_off_x() { return 2 * kWeightBoxBytes; }
+__host__ __device__ constexpr int stage_off_s(int act, int MT) {
+  return stage_off_x() + x_boxes(act) * 128 * 8 * MT;
+}
+__host__ __device__ constexpr int stage_off_b(int act, int MT) {
+  return stage_off_s(act, MT) + kBN * 16;
+}
+__host__ __device__ constexpr int stage_bytes(int act, int MT) {
+  return (stage_off_b(act, MT) + kBN * 16 + 1023) / 1024 * 1024;
+}
+
+// x-table variant (16-bit x, M <= 8): the stage holds codes, scales and
+// biases only; x lives in a per-block table converted once at block start.
+__host__ __device__ constexpr int xt_stage_off_s() { return 2 * kWeightBoxBytes; }
+__host__ __device__ constexpr int xt_stage_bytes() {
+  return (xt_stage_off_s() + 2 * kBN * 16 + 1023) / 1024 * 1024;
+}
+// x table [K/64 groups][8 rows][128 B] fp16 + T and U tables [K/64][8] fp32 +
+// per-row 1/f [8] fp32 + per-row max bits [8] u32.
+__host__ __device__ constexpr int xt_table_bytes(int K) { return (K / 64) * 1024 + 2 * (K / 64) * 32 + 64; }
+constexpr int kMaxXtBytes = 96 * 1024;
+
+// Bytes of the per-block table of group sums X_g[m]: [K/64][8*MT] fp32.
+__host__ __device__ constexpr int xsum_bytes(int K, int MT) { return (K / 64) * 8 * MT * 4; }
+constexpr int kMaxXsumBytes = 32 * 1024;
 
 struct GemmParams {
+  const void* x;    // activations in global memory (for the group sums)
   int M, K, N;
   int KT;           // stages along the full K
   int S;            // K splits per row block (1 = no split)
   int n_units;      // row blocks * S
   int D;            // pipeline depth (stages in the shared-memory ring)
   int stage_bytes;
-  int off_x, off_s, off_b, off_xs;   // offsets inside a stage (codes at 0)
-  int xbox_bytes;   // shared-memory stride between the x boxes of a stage
+  int off_x, off_s, off_b;   // offsets inside a stage (codes at 0)
+  int xt;           // 1: x-table variant (no x in the stages)
+  int tab_bytes;    // bytes of the table region after the stage ring (1 KiB multiple)
+  int x3d;          // 1: x arrives as one 3-D box per stage, 0: one box per group
+                    // (same shared-memory layout either way: [group][8*MT rows][128 B],
+                    // rows >= M zero-filled by the copy)
   uint32_t tx_bytes;
   void* y;
   float* part;                 // split-K partials [S][M][N]
@@ -114,35 +161,33 @@ int launch_gemm_f32(const GemmLaunch& L);
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, int32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-      *abort_flag = 1;
-      atomicOr(err, kErrWaitTimeout);
-      return false;
+    if ((it & 63u) == 0u) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitTimeoutCycles) {
+        *abort_flag = 1;
+        atomicOr(err, kErrWaitTimeout);
+        return false;
+      }
     }
   }
 }
 
 // A wait that ignores the abort flag (used to let issued copies land).
 __device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, int32_t* err) {
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (clock64() - t0 > kWaitTimeoutCycles) {
       atomicOr(err, kErrWaitTimeout);
       return;
     }
   }
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Codes (i, i+4) of a word as a bf16x2 / f16x2 pair. With kExact the pair is
-// (q_i, q_{i+4}); otherwise it is (M + q_i, M + q_{i+4}) with M = 128 (bf16)
+// (q_i, q_{i+4}); otherwise it is (B + q_i, B + q_{i+4}) with B = 128 (bf16)
 // or 1024 (f16), one AND/OR and no arithmetic.
 template <bool kF16, bool kExact>
 __device__ __forceinline__ uint32_t code_pair(uint32_t word, int i) {
@@ -161,10 +206,33 @@ __device__ __forceinline__ uint32_t code_pair(uint32_t word, int i) {
   }
 }
 
-// Element j (0..3) of four packed bf16 values, widened exactly to fp32.
-__device__ __forceinline__ float bf16_at(const uint2& v, int j) {
-  const uint32_t w = (j >> 1) ? v.y : v.x;
-  return __uint_as_float((j & 1) ? (w & 0xFFFF0000u) : (w << 16));
+// GPW consecutive bf16 values (4, 8 or 16 bytes) as packed words.
+template <int GPW>
+struct Packed {
+  uint32_t w[GPW / 2];
+};
+template <int GPW>
+__device__ __forceinline__ Packed<GPW> lds_packed(const uint8_t* ptr) {
+  Packed<GPW> r;
+  if constexpr (GPW == 2) {
+    r.w[0] = *reinterpret_cast<const uint32_t*>(ptr);
+  } else if constexpr (GPW == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(ptr);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(ptr);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+    r.w[2] = v.z;
+    r.w[3] = v.w;
+  }
+  return r;
+}
+template <int GPW>
+__device__ __forceinline__ float bf16_of(const Packed<GPW>& p, int jj) {
+  const uint32_t w = p.w[jj >> 1];
+  return __uint_as_float((jj & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
 // fp32 x as the exact sum of three bf16 terms, packed as (a, b) pairs.
@@ -209,209 +277,492 @@ __device__ __forceinline__ bool better(float v, uint32_t n, bool has, float bv, 
   return v > bv || (v == bv && n < bn);
 }
 
-// Four groups (4kh .. 4kh+3) of one 512-wide stage for this thread's weight
-// rows r0, r0+1: totals += scale * A_g + bias * X_g per group.
+// Per-thread constants of a consumer: 32-bit shared-memory offsets that do
+// not change from stage to stage (the rest of each address is an immediate).
 template <int ACT, int MT>
-__device__ __forceinline__ void consume_stage(const uint8_t* st, const GemmParams& p, int rt,
-                                              int kh, int g, int t, float (&tot)[MT][4]) {
+struct LaneOffsets {
+  uint32_t w_even, w_odd;   // codes of this thread's even / odd weight row, tile 0
+  uint32_t g3x32;           // (g % 4) * 32: the row-dependent part of the swizzle
+  uint32_t x_h0, x_h1;      // x: the chunk of row g, first group of the slice, for
+                            // k-halves h = 0, 1 (16-bit x); line and chunk (fp32 x)
+  uint32_t sc;              // scales of the even row of tile 0 for this K-slice
+  uint32_t xs;              // (first group of the slice, row 2t) in the group-sum table, bytes
+};
+
+template <int ACT, int MT>
+__device__ __forceinline__ LaneOffsets<ACT, MT> lane_offsets(int rw, int kq, int g, int t) {
+  using C = Cfg<MT>;
+  constexpr int MP = 8 * MT;
+  LaneOffsets<ACT, MT> o;
+  const int row = 16 * (C::RT * rw) + 2 * g;               // even row of tile 0
+  const int box = (C::GPW == 4) ? kq * kWeightBoxBytes : 0;
+  o.w_even = box + row * 128 + ((t >> 1) << 4) + ((t & 1) << 3);
+  o.w_odd = box + (row + 1) * 128 + (((t >> 1) ^ 1) << 4) + ((t & 1) << 3);
+  o.g3x32 = (uint32_t)(g & 3) << 5;
+  if constexpr (ACT == VQ_F32) {
+    // line (half-group 2j + t/2, row g) and the swizzled chunk 4(t&1) ^ g
+    const int hg0 = 2 * (kq * C::GPW) + (t >> 1);
+    o.x_h0 = stage_off_x() + (hg0 * MP + g) * 128;
+    o.x_h1 = (uint32_t)((4 * (t & 1)) ^ g) << 4;
+  } else {
+    const int j0 = kq * C::GPW;
+    o.x_h0 = stage_off_x() + (j0 * MP + g) * 128 + (((2 * t) ^ g) << 4);
+    o.x_h1 = stage_off_x() + (j0 * MP + g) * 128 + (((2 * t + 1) ^ g) << 4);
+  }
+  o.sc = stage_off_s(ACT, MT) + row * 16 + kq * C::GPW * 2;
+  o.xs = (uint32_t)((kq * C::GPW * MP + 2 * t) * 4);
+  return o;
+}
+
+template <int GPW, int kOff>
+__device__ __forceinline__ Packed<GPW> lds_packed_at(uint32_t a) {
+  Packed<GPW> r;
+  if constexpr (GPW == 4) {
+    const uint2 v = lds64<kOff>(a);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+  } else {
+    const uint4 v = lds128<kOff>(a);
+    r.w[0] = v.x;
+    r.w[1] = v.y;
+    r.w[2] = v.z;
+    r.w[3] = v.w;
+  }
+  return r;
+}
+
+// This warp's share of one stage: groups kq*GPW .. kq*GPW+GPW-1 for its RT
+// row tiles. MMA row i of tile r is weight row 16r + 2i, MMA row i+8 is
+// weight row 16r + 2i + 1. sb is the stage's shared address, xsb the group-sum
+// table's shared address for the stage's first group. All per-tile, per-group
+// and per-row offsets are load immediates.
+template <int ACT, int MT>
+__device__ __forceinline__ void consume_stage(uint32_t sb, uint32_t xsb,
+                                              const LaneOffsets<ACT, MT>& o,
+                                              float (&tot)[Cfg<MT>::RT][MT][4]) {
+  using C = Cfg<MT>;
+  constexpr int RT = C::RT, GPW = C::GPW, MP = 8 * MT;
   constexpr bool kF16 = (ACT == VQ_F16);
   constexpr bool kF32 = (ACT == VQ_F32);
-  constexpr int MP = 8 * MT;
+  constexpr int kBiasOff = kBN * 16;   // biases follow the scales
+  static_assert(GPW == 4 || GPW == 8, "K-slices of 4 or 8 groups");
   // codes enter the MMA as (offset + q) except for fp32 activations
   constexpr float kOffset = kF32 ? 0.f : (kF16 ? 1024.f : 128.f);
-  const int r0 = 16 * rt + 2 * g;   // weight rows r0 (MMA row g) and r0+1 (MMA row g+8)
-  const uint2 sv0 = *reinterpret_cast<const uint2*>(st + p.off_s + r0 * 16 + kh * 8);
-  const uint2 sv1 = *reinterpret_cast<const uint2*>(st + p.off_s + (r0 + 1) * 16 + kh * 8);
-  const uint2 bv0 = *reinterpret_cast<const uint2*>(st + p.off_b + r0 * 16 + kh * 8);
-  const uint2 bv1 = *reinterpret_cast<const uint2*>(st + p.off_b + (r0 + 1) * 16 + kh * 8);
-  const float* xs = reinterpret_cast<const float*>(st + p.off_xs);
-  const uint8_t* wbox = st + kh * kWeightBoxBytes;   // groups 4kh .. 4kh+3
-  const int sw0 = r0 & 7, sw1 = (r0 + 1) & 7;        // 128-byte swizzle of the two rows
 
-#pragma unroll
-  for (int jj = 0; jj < 4; ++jj) {
-    const int j = 4 * kh + jj;
-    const int cw = 2 * jj + (t >> 1);                 // 16-byte chunk of words 2t, 2t+1
-    const uint2 wa = *reinterpret_cast<const uint2*>(wbox + r0 * 128 + ((cw ^ sw0) << 4) +
-                                                     ((t & 1) << 3));
-    const uint2 wb = *reinterpret_cast<const uint2*>(wbox + (r0 + 1) * 128 + ((cw ^ sw1) << 4) +
-                                                     ((t & 1) << 3));
-    float acc[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  Packed<GPW> sc0[RT], sc1[RT], bi0[RT], bi1[RT];
+  const uint32_t sa = sb + o.sc;
+  static_for<RT>([&](auto rc) {
+    constexpr int r = decltype(rc)::value;
+    sc0[r] = lds_packed_at<GPW, 256 * r>(sa);
+    sc1[r] = lds_packed_at<GPW, 256 * r + 16>(sa);
+    bi0[r] = lds_packed_at<GPW, 256 * r + kBiasOff>(sa);
+    bi1[r] = lds_packed_at<GPW, 256 * r + kBiasOff + 16>(sa);
+  });
+  const uint32_t we = sb + o.w_even, wo = sb + o.w_odd;
+  const uint32_t xa0 = sb + o.x_h0, xa1 = sb + o.x_h1;
 
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t qa = h ? wa.y : wa.x;
-      const uint32_t qb = h ? wb.y : wb.x;
-      if constexpr (!kF32) {
-        // x[m][64j + 16t + 8h + i], stored by the helper as the fragment
-        // pairs (x0,x4) (x1,x5) (x2,x6) (x3,x7)
-        uint4 xv[MT];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const int m = 8 * mt + g;
-          xv[mt] = make_uint4(0u, 0u, 0u, 0u);
-          if (m < p.M)
-            xv[mt] = *reinterpret_cast<const uint4*>(st + p.off_x + j * p.xbox_bytes + m * 128 +
-                                                     (((2 * t + h) ^ g) << 4));
+  static_for<GPW>([&](auto jc) {
+    constexpr int jj = decltype(jc)::value;
+    // codes: 16-byte chunk (2*(j%4) + t/2) of the row, XOR-swizzled by row % 8;
+    // tile r is 16 rows (2 KiB) further, groups 4..7 (GPW = 8) in box 1
+    constexpr int kBox = (GPW == 8 && jj >= 4) ? kWeightBoxBytes : 0;
+    const uint32_t sw = ((uint32_t)((jj & 3) << 5)) ^ o.g3x32;
+    const uint32_t ae = we + sw, ao = wo + sw;
+    uint2 wa[RT], wb[RT];
+    static_for<RT>([&](auto rc) {
+      constexpr int r = decltype(rc)::value;
+      wa[r] = lds64<kBox + 2048 * r>(ae);
+      wb[r] = lds64<kBox + 2048 * r>(ao);
+    });
+    float acc[RT][MT][4];
+
+    static_for<2>([&](auto hc) {
+      constexpr int h = decltype(hc)::value;
+      // B fragments of rows m = 8mt + g for k = 16t + 8h + (0..7):
+      // bx[mt][s'][0..1] = (x_{2s'}, x_{2s'+4}), (x_{2s'+1}, x_{2s'+5})
+      uint32_t bx[MT][2][2];
+      uint32_t bxm[MT][2][2], bxl[MT][2][2];   // fp32 only: middle / low terms
+      static_for<MT>([&](auto mc) {
+        constexpr int mt = decltype(mc)::value;
+        if constexpr (!kF32) {
+          const uint4 v = lds128<(jj * MP + 8 * mt) * 128>(h ? xa1 : xa0);
+          bx[mt][0][0] = prmt(v.x, v.z, 0x5410u);
+          bx[mt][0][1] = prmt(v.x, v.z, 0x7632u);
+          bx[mt][1][0] = prmt(v.y, v.w, 0x5410u);
+          bx[mt][1][1] = prmt(v.y, v.w, 0x7632u);
+        } else {
+          // chunks 4(t&1) + 2h and that + 1 of line (half-group, row): x_h0
+          // holds the line, x_h1 the swizzled chunk (4(t&1) ^ g) << 4
+          const uint32_t c0 = xa0 + (o.x_h1 ^ (32u * h));
+          const uint4 u0 = lds128<(2 * jj * MP + 8 * mt) * 128>(c0);
+          const uint4 u1 = lds128<(2 * jj * MP + 8 * mt) * 128>(xa0 + ((o.x_h1 ^ (32u * h)) ^ 16u));
+          split3(__uint_as_float(u0.x), __uint_as_float(u1.x), bx[mt][0][0], bxm[mt][0][0], bxl[mt][0][0]);
+          split3(__uint_as_float(u0.y), __uint_as_float(u1.y), bx[mt][0][1], bxm[mt][0][1], bxl[mt][0][1]);
+          split3(__uint_as_float(u0.z), __uint_as_float(u1.z), bx[mt][1][0], bxm[mt][1][0], bxl[mt][1][0]);
+          split3(__uint_as_float(u0.w), __uint_as_float(u1.w), bx[mt][1][1], bxm[mt][1][1], bxl[mt][1][1]);
         }
+      });
 #pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const bool first = (h == 0 && s2 == 0);
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+          const uint32_t qa = h ? wa[r].y : wa[r].x;
+          const uint32_t qb = h ? wb[r].y : wb[r].x;
           uint32_t a[4];
-          a[0] = code_pair<kF16, false>(qa, 2 * s2);
-          a[1] = code_pair<kF16, false>(qb, 2 * s2);
-          a[2] = code_pair<kF16, false>(qa, 2 * s2 + 1);
-          a[3] = code_pair<kF16, false>(qb, 2 * s2 + 1);
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            mma_16816<kF16>(acc[mt], a, s2 ? xv[mt].z : xv[mt].x, s2 ? xv[mt].w : xv[mt].y);
-        }
-      } else {
-        // fp32 x: half-group boxes of 32 values; this thread's 8 values are
-        // chunks c, c+1 of line m in box 2j + t/2
-        float4 x0[MT], x1[MT];
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          const int m = 8 * mt + g;
-          const int c = 4 * (t & 1) + 2 * h;
-          x0[mt] = x1[mt] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (m < p.M) {
-            const uint8_t* line = st + p.off_x + (2 * j + (t >> 1)) * p.xbox_bytes + m * 128;
-            x0[mt] = *reinterpret_cast<const float4*>(line + ((c ^ g) << 4));
-            x1[mt] = *reinterpret_cast<const float4*>(line + (((c + 1) ^ g) << 4));
-          }
-        }
-#pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-          uint32_t a[4];
-          a[0] = code_pair<false, true>(qa, 2 * s2);
-          a[1] = code_pair<false, true>(qb, 2 * s2);
-          a[2] = code_pair<false, true>(qa, 2 * s2 + 1);
-          a[3] = code_pair<false, true>(qb, 2 * s2 + 1);
+          a[0] = code_pair<kF16, kF32>(qa, 2 * s2);
+          a[1] = code_pair<kF16, kF32>(qb, 2 * s2);
+          a[2] = code_pair<kF16, kF32>(qa, 2 * s2 + 1);
+          a[3] = code_pair<kF16, kF32>(qb, 2 * s2 + 1);
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            const float e0 = s2 ? x0[mt].z : x0[mt].x;   // x_{2s'}
-            const float e4 = s2 ? x1[mt].z : x1[mt].x;   // x_{2s'+4}
-            const float e1 = s2 ? x0[mt].w : x0[mt].y;   // x_{2s'+1}
-            const float e5 = s2 ? x1[mt].w : x1[mt].y;   // x_{2s'+5}
-            uint32_t b0h, b0m, b0l, b1h, b1m, b1l;
-            split3(e0, e4, b0h, b0m, b0l);
-            split3(e1, e5, b1h, b1m, b1l);
-            mma_16816<false>(acc[mt], a, b0h, b1h);
-            mma_16816<false>(acc[mt], a, b0m, b1m);
-            mma_16816<false>(acc[mt], a, b0l, b1l);
-          }
-        }
-      }
-    }
-
-    // fold group j: scale the code sums; the bias term (less the code
-    // offset) multiplies the group sum of x
-    const float s_a = bf16_at(sv0, jj), s_b = bf16_at(sv1, jj);
-    const float c_a = fmaf(-kOffset, s_a, bf16_at(bv0, jj));
-    const float c_b = fmaf(-kOffset, s_b, bf16_at(bv1, jj));
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      const float2 xsum = *reinterpret_cast<const float2*>(xs + j * MP + 8 * mt + 2 * t);
-      tot[mt][0] = fmaf(s_a, acc[mt][0], fmaf(c_a, xsum.x, tot[mt][0]));
-      tot[mt][1] = fmaf(s_a, acc[mt][1], fmaf(c_a, xsum.y, tot[mt][1]));
-      tot[mt][2] = fmaf(s_b, acc[mt][2], fmaf(c_b, xsum.x, tot[mt][2]));
-      tot[mt][3] = fmaf(s_b, acc[mt][3], fmaf(c_b, xsum.y, tot[mt][3]));
-    }
-  }
-}
-
-// Helper work on one landed stage: X_g[m] for every group and row, and (for
-// 16-bit x) each 16-byte chunk of x rewritten in place as the fragment pairs
-// (x0,x4) (x1,x5) (x2,x6) (x3,x7).
-template <int ACT, int MT>
-__device__ __forceinline__ void prepare_stage(uint8_t* st, const GemmParams& p, int lane) {
-  constexpr int MP = 8 * MT;
-  float* xs = reinterpret_cast<float*>(st + p.off_xs);
-  for (int idx = lane; idx < 8 * MP; idx += 32) {
-    const int j = idx / MP, m = idx - (idx / MP) * MP;
-    float s = 0.f;
-    if (m < p.M) {
-      if constexpr (ACT == VQ_F32) {
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          const uint8_t* line = st + p.off_x + (2 * j + hb) * p.xbox_bytes + m * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const float4 v = *reinterpret_cast<const float4*>(line + ((c ^ (m & 7)) << 4));
-            s += v.x;
-            s += v.y;
-            s += v.z;
-            s += v.w;
-          }
-        }
-      } else {
-        uint8_t* line = st + p.off_x + j * p.xbox_bytes + m * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4* ptr = reinterpret_cast<uint4*>(line + ((c ^ (m & 7)) << 4));
-          const uint4 v = *ptr;
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if constexpr (ACT == VQ_F16) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-              s += f.x;
-              s += f.y;
-            } else {
-              s += __uint_as_float(w[e] << 16);
-              s += __uint_as_float(w[e] & 0xFFFF0000u);
+            if (first)
+              mma_16816_zc<kF16>(acc[r][mt], a, bx[mt][s2][0], bx[mt][s2][1]);
+            else
+              mma_16816<kF16>(acc[r][mt], a, bx[mt][s2][0], bx[mt][s2][1]);
+            if constexpr (kF32) {
+              mma_16816<false>(acc[r][mt], a, bxm[mt][s2][0], bxm[mt][s2][1]);
+              mma_16816<false>(acc[r][mt], a, bxl[mt][s2][0], bxl[mt][s2][1]);
             }
           }
-          *ptr = make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
-                            prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
         }
       }
+    });
+
+    // fold group jj: scale the code sums; the bias term (less the code
+    // offset) multiplies the group sum of x, rows 8mt+2t and 8mt+2t+1
+    float2 xs[MT];
+    static_for<MT>([&](auto mc) {
+      constexpr int mt = decltype(mc)::value;
+      const uint2 v = lds64<(jj * MP + 8 * mt) * 4>(xsb);
+      xs[mt] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+    });
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+      const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
+      const float c_a = fmaf(-kOffset, s_a, bf16_of(bi0[r], jj));
+      const float c_b = fmaf(-kOffset, s_b, bf16_of(bi1[r], jj));
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        tot[r][mt][0] = fmaf(s_a, acc[r][mt][0], fmaf(c_a, xs[mt].x, tot[r][mt][0]));
+        tot[r][mt][1] = fmaf(s_a, acc[r][mt][1], fmaf(c_a, xs[mt].y, tot[r][mt][1]));
+        tot[r][mt][2] = fmaf(s_b, acc[r][mt][2], fmaf(c_b, xs[mt].x, tot[r][mt][2]));
+        tot[r][mt][3] = fmaf(s_b, acc[r][mt][3], fmaf(c_b, xs[mt].y, tot[r][mt][3]));
+      }
     }
-    xs[idx] = s;
-  }
-  // the slot is refilled by TMA (async proxy) after these generic writes
-  fence_proxy_async_smem();
+  });
 }
 
-template <int ACT, int MT, bool ARGMAX>
-__global__ void __launch_bounds__(threads_for(MT), 1)
+// The block's table of group sums X_g[m] = sum of x[m][64g .. 64g+63] for all
+// K/64 groups, laid out [K/64][8*MT] (rows m >= M are 0). Every 16-byte chunk
+// of x is read once, eight loads in flight per thread; the chunks of one
+// group are summed across lanes.
+template <int ACT>
+__device__ __forceinline__ float chunk_sum(const uint4& v) {
+  if constexpr (ACT == VQ_F32) {
+    return (__uint_as_float(v.x) + __uint_as_float(v.y)) +
+           (__uint_as_float(v.z) + __uint_as_float(v.w));
+  } else {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float a[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if constexpr (ACT == VQ_F16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+        a[e] = f.x + f.y;
+      } else {
+        a[e] = __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+      }
+    }
+    return (a[0] + a[1]) + (a[2] + a[3]);
+  }
+}
+
+template <int ACT, int MT>
+__device__ __forceinline__ void build_xsum(float* xsum, const GemmParams& p, int warp, int lane,
+                                           int n_warps) {
+  constexpr int MP = 8 * MT;
+  constexpr int CPG = (ACT == VQ_F32) ? 16 : 8;   // 16-byte chunks per group
+  constexpr int PPW = 32 / CPG;                   // (group, row) pairs per warp step
+  constexpr int kBatch = 8;                       // loads in flight per thread
+  const int KG = p.K / 64;
+  const int pairs = KG * MP;
+  const int chunk = lane % CPG;
+  const int step = n_warps * PPW;
+  const size_t eb = (ACT == VQ_F32) ? 4 : 2;
+  for (int base = warp * PPW; base < pairs; base += step * kBatch) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int pair = base + b * step + lane / CPG;
+      const int gi = pair / MP, m = pair - (pair / MP) * MP;
+      v[b] = make_uint4(0u, 0u, 0u, 0u);
+      if (pair < pairs && m < p.M)
+        v[b] = __ldg(reinterpret_cast<const uint4*>(
+            static_cast<const uint8_t*>(p.x) + ((size_t)m * p.K + (size_t)gi * 64) * eb +
+            chunk * 16));
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int pair = base + b * step + lane / CPG;
+      float s = chunk_sum<ACT>(v[b]);
+#pragma unroll
+      for (int off = CPG / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (chunk == 0 && pair < pairs) xsum[pair] = s;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- x table
+// For 16-bit x and M <= 8 the block converts x once, while its first stages
+// are in flight, into an fp16 table laid out as MMA B fragments:
+//   line (group gi, row m) = 128 bytes = 8 chunks; chunk c (holding k =
+//   64gi + 8c .. +7) sits at position c ^ m and stores the fp16 pairs
+//   (x'0,x'4) (x'1,x'5) (x'2,x'6) (x'3,x'7), where x'_i = x_i * f_m * phi_i,
+//   phi_i = 1 for even i and 1/16 for odd i, and f_m = 2^(13 - floor(log2
+//   max|x_m|)) so that every |x'| < 2^14 (no fp16 overflow, whatever the
+//   scale of the activations).
+// With codes entered as the fp16 values 1024 + q (even i) and 1024 + 16q (odd
+// i), taken straight from nibble positions 0-3 and 4-7 of each byte pair,
+// each MMA product is (1024 + q) x' or (1024 + 16q) x'/16 scaled by f_m, so
+//   acc_g = f_m * sum_g q x + U_g,  U_g = 1024 * sum_g x'
+// and the group folds as  tot += s * (acc_g - U_g) + b * T_g,  T_g = f_m * sum_g x,
+// with y = tot / f_m at the end.
+struct XTab {
+  uint32_t lines;   // shared address of the fp16 table
+  float* T;         // [K/64][8]
+  float* U;         // [K/64][8]
+  float* inv_f;     // [8]
+  uint32_t* rmax;   // [8] float bits of max |x_m|
+};
+
+template <int ACT>
+__device__ __forceinline__ float x_at(const uint4& v, int i) {
+  const uint32_t w = (i >> 1) == 0 ? v.x : (i >> 1) == 1 ? v.y : (i >> 1) == 2 ? v.z : v.w;
+  if constexpr (ACT == VQ_F16) {
+    const __half2 h = *reinterpret_cast<const __half2*>(&w);
+    return (i & 1) ? __high2float(h) : __low2float(h);
+  } else {
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+}
+
+__device__ __forceinline__ float row_scale(uint32_t rmax_bits) {
+  // 2^(13 - floor(log2 max)); 1 for an all-zero row
+  if (rmax_bits == 0u) return 1.f;
+  const int e = (int)(rmax_bits >> 23);
+  const int fe = 267 - e;   // biased exponent of the scale
+  return __uint_as_float((uint32_t)(fe > 254 ? 254 : fe) << 23);
+}
+
+template <int ACT>
+__device__ __forceinline__ void build_xtab(uint8_t* tab_gen, const XTab& X, const GemmParams& p,
+                                           int tid, int n_threads, uint32_t bar_threads) {
+  // x is already in place (raw 16-bit values, lines swizzled) from the TMA
+  const int KG = p.K / 64;
+  const int chunks = KG * 64;   // 8 rows x 8 chunks per group
+  // pass A: per-(group,row) even / odd sums and the row maxima
+  for (int base = tid; base - tid < chunks; base += n_threads) {
+    const int ci = base;
+    const int m = (ci >> 3) & 7, gi = ci >> 6, c = ci & 7;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (ci < chunks) v = *reinterpret_cast<const uint4*>(tab_gen + (gi * 8 + m) * 128 + ((c ^ m) << 4));
+    float se = 0.f, so = 0.f, mx = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float xv = x_at<ACT>(v, i);
+      if (i & 1) so += xv; else se += xv;
+      mx = fmaxf(mx, fabsf(xv));
+    }
+    // the 8 chunks of a (group, row) line are 8 consecutive lanes
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      se += __shfl_xor_sync(0xffffffffu, se, off);
+      so += __shfl_xor_sync(0xffffffffu, so, off);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (ci < chunks && c == 0) {
+      X.T[gi * 8 + m] = se;
+      X.U[gi * 8 + m] = so;
+      atomicMax(X.rmax + m, __float_as_uint(mx));
+    }
+  }
+  named_bar_sync(1, bar_threads);
+  // pass B: scale and convert in place; turn the sums into T and U
+  for (int ci = tid; ci < chunks; ci += n_threads) {
+    const int m = (ci >> 3) & 7, gi = ci >> 6, c = ci & 7;
+    const float f = row_scale(X.rmax[m]);
+    uint4* ptr = reinterpret_cast<uint4*>(tab_gen + (gi * 8 + m) * 128 + ((c ^ m) << 4));
+    const uint4 v = *ptr;
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float ph = (i & 1) ? 0.0625f : 1.f;
+      const __half2 hp = __floats2half2_rn(x_at<ACT>(v, i) * f * ph, x_at<ACT>(v, i + 4) * f * ph);
+      o[i] = *reinterpret_cast<const uint32_t*>(&hp);
+    }
+    *ptr = make_uint4(o[0], o[1], o[2], o[3]);
+    if (c == 0) {
+      const float se = X.T[gi * 8 + m], so = X.U[gi * 8 + m];
+      X.T[gi * 8 + m] = f * (se + so);
+      X.U[gi * 8 + m] = 1024.f * f * (se + 0.0625f * so);
+    }
+  }
+  if (tid < 8) X.inv_f[tid] = 1.f / row_scale(X.rmax[tid]);
+  named_bar_sync(1, bar_threads);
+}
+
+// Per-thread constants of the x-table consumer.
+struct XtLane {
+  uint32_t w_even, w_odd;   // codes of the even / odd weight row of tile 0
+  uint32_t g3x32;           // (g % 4) * 32
+  uint32_t x_h0, x_h1;      // table chunk (group 0 of the slice, row g) for h = 0, 1
+  uint32_t sc;              // scales of the even row of tile 0 for the slice
+  uint32_t ts;              // byte offset of (first group of the slice, row 2t) in T / U
+};
+
+template <int MT>
+__device__ __forceinline__ XtLane xt_lane(uint32_t lines, int rw, int kq, int g, int t) {
+  using C = Cfg<MT>;
+  XtLane o;
+  const int row = 16 * (C::RT * rw) + 2 * g;
+  const int box = (C::GPW == 4) ? kq * kWeightBoxBytes : 0;
+  o.w_even = box + row * 128 + ((t >> 1) << 4) + ((t & 1) << 3);
+  o.w_odd = box + (row + 1) * 128 + (((t >> 1) ^ 1) << 4) + ((t & 1) << 3);
+  o.g3x32 = (uint32_t)(g & 3) << 5;
+  const int j0 = kq * C::GPW;
+  o.x_h0 = lines + (j0 * 8 + g) * 128 + (((2 * t) ^ g) << 4);
+  o.x_h1 = lines + (j0 * 8 + g) * 128 + (((2 * t + 1) ^ g) << 4);
+  o.sc = xt_stage_off_s() + row * 16 + kq * C::GPW * 2;
+  o.ts = (uint32_t)((j0 * 8 + 2 * t) * 4);
+  return o;
+}
+
+// One stage of the x-table variant (MT = 1): groups kq*GPW .. +GPW-1 of
+// stage kt for the warp's RT row tiles.
+template <int ACT>
+__device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T_a, uint32_t U_a,
+                                                 const XtLane& o,
+                                                 float (&tot)[Cfg<1>::RT][1][4]) {
+  using C = Cfg<1>;
+  constexpr int RT = C::RT, GPW = C::GPW;
+  constexpr int kBiasOff = kBN * 16;
+  constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0 in both halves
+  static_assert(GPW == 4 || GPW == 8, "K-slices of 4 or 8 groups");
+
+  Packed<GPW> sc0[RT], sc1[RT], bi0[RT], bi1[RT];
+  const uint32_t sa = sb + o.sc;
+  static_for<RT>([&](auto rc) {
+    constexpr int r = decltype(rc)::value;
+    sc0[r] = lds_packed_at<GPW, 256 * r>(sa);
+    sc1[r] = lds_packed_at<GPW, 256 * r + 16>(sa);
+    bi0[r] = lds_packed_at<GPW, 256 * r + kBiasOff>(sa);
+    bi1[r] = lds_packed_at<GPW, 256 * r + kBiasOff + 16>(sa);
+  });
+  const uint32_t we = sb + o.w_even, wo = sb + o.w_odd;
+  const uint32_t xg = (uint32_t)kt * 8 * 1024;   // the stage's first group in the x table
+  const uint32_t xa0 = o.x_h0 + xg, xa1 = o.x_h1 + xg;
+  const uint32_t ta = T_a + (uint32_t)kt * 8 * 32, ua = U_a + (uint32_t)kt * 8 * 32;
+
+  static_for<GPW>([&](auto jc) {
+    constexpr int jj = decltype(jc)::value;
+    constexpr int kBox = (GPW == 8 && jj >= 4) ? kWeightBoxBytes : 0;
+    const uint32_t sw = ((uint32_t)((jj & 3) << 5)) ^ o.g3x32;
+    const uint32_t ae = we + sw, ao = wo + sw;
+    uint2 wa[RT], wb[RT];
+    static_for<RT>([&](auto rc) {
+      constexpr int r = decltype(rc)::value;
+      wa[r] = lds64<kBox + 2048 * r>(ae);
+      wb[r] = lds64<kBox + 2048 * r>(ao);
+    });
+    float acc[RT][4];
+    static_for<2>([&](auto hc) {
+      constexpr int h = decltype(hc)::value;
+      const uint4 bx = lds128<jj * 1024>(h ? xa1 : xa0);
+#pragma unroll
+      for (int r = 0; r < RT; ++r) {
+        const uint32_t qa = h ? wa[r].y : wa[r].x;
+        const uint32_t qb = h ? wb[r].y : wb[r].x;
+        const uint32_t qa8 = qa >> 8, qb8 = qb >> 8;
+        // step s' = 0: pairs (c0,c4) and (c1,c5); s' = 1: (c2,c6) and (c3,c7)
+        const uint32_t a0[4] = {lop3_and_or(qa, 0x000F000Fu, kMagic), lop3_and_or(qb, 0x000F000Fu, kMagic),
+                                lop3_and_or(qa, 0x00F000F0u, kMagic), lop3_and_or(qb, 0x00F000F0u, kMagic)};
+        const uint32_t a1[4] = {lop3_and_or(qa8, 0x000F000Fu, kMagic), lop3_and_or(qb8, 0x000F000Fu, kMagic),
+                                lop3_and_or(qa8, 0x00F000F0u, kMagic), lop3_and_or(qb8, 0x00F000F0u, kMagic)};
+        float (&d)[4] = acc[r];
+        if (h == 0)
+          mma_16816_zc<true>(d, a0, bx.x, bx.y);
+        else
+          mma_16816<true>(d, a0, bx.x, bx.y);
+        mma_16816<true>(d, a1, bx.z, bx.w);
+      }
+    });
+    // fold: tot += s * (acc - U) + b * T, rows 2t and 2t+1 of the block
+    const uint2 tv = lds64<jj * 32>(ta), uv = lds64<jj * 32>(ua);
+    const float T0 = __uint_as_float(tv.x), T1 = __uint_as_float(tv.y);
+    const float U0 = __uint_as_float(uv.x), U1 = __uint_as_float(uv.y);
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+      const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
+      const float b_a = bf16_of(bi0[r], jj), b_b = bf16_of(bi1[r], jj);
+      tot[r][0][0] = fmaf(s_a, acc[r][0], fmaf(b_a, T0, fmaf(-s_a, U0, tot[r][0][0])));
+      tot[r][0][1] = fmaf(s_a, acc[r][1], fmaf(b_a, T1, fmaf(-s_a, U1, tot[r][0][1])));
+      tot[r][0][2] = fmaf(s_b, acc[r][2], fmaf(b_b, T0, fmaf(-s_b, U0, tot[r][0][2])));
+      tot[r][0][3] = fmaf(s_b, acc[r][3], fmaf(b_b, T1, fmaf(-s_b, U1, tot[r][0][3])));
+    }
+  });
+}
+
+template <int ACT, int MT, bool ARGMAX, bool XT>
+__global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     vq_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_x,
                    const GemmParams p) {
+  using C = Cfg<MT>;
   constexpr int MP = 8 * MT;
-  constexpr int KH = kh_for(MT);
-  constexpr int kConsumers = kRowTiles * KH;          // consumer warps
+  constexpr int RT = C::RT, KQ = C::KQ, RW = C::RW, TEAMS = C::TEAMS, SLICES = C::SLICES;
+  constexpr int kConsumers = C::WARPS;
   constexpr int kProducerWarp = kConsumers;
-  constexpr int kHelperWarp = kConsumers + 1;
-  constexpr int kXBoxes = (ACT == VQ_F32) ? 16 : 8;
+  constexpr int kXBoxes = (ACT == VQ_F32) ? 16 : 8;   // per-group boxes (x3d == 0)
   constexpr int kXBoxElems = kBK / kXBoxes;
-  constexpr uint32_t kEpiThreads = kRowTiles * 32;     // the K-half-0 consumers
+  constexpr uint32_t kEpiThreads = RW * 32;            // the K-slice-0 consumers
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const sbase = smem_raw + (base - raw);
-  uint8_t* const misc = sbase + p.D * p.stage_bytes;
-  const uint32_t misc_a = base + p.D * p.stage_bytes;
+  // [D stages][tables: x table (x-table variant) or group sums][misc][K-slice partials]
+  uint8_t* const tabs = sbase + p.D * p.stage_bytes;
+  uint8_t* const misc = tabs + p.tab_bytes;
+  const uint32_t misc_a = base + p.D * p.stage_bytes + p.tab_bytes;
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 192);
   volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 196);
   float* const red_v = reinterpret_cast<float*>(misc + 256);
-  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + kRowTiles * 64 * 4);
-  float* const red_k = reinterpret_cast<float*>(misc + kMiscBytes);   // K-half partials
+  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + 8 * 64 * 4);
+  float* const red_k = reinterpret_cast<float*>(misc + kMiscBytes);   // [SLICES-1][128][MP]
+  float* const xsum = reinterpret_cast<float*>(tabs);   // [K/64][MP]
+  const int KG = p.K / 64;
+  XTab X;
+  X.lines = smem_addr(tabs);
+  X.T = reinterpret_cast<float*>(tabs + KG * 1024);
+  X.U = X.T + KG * 8;
+  X.inv_f = X.U + KG * 8;
+  X.rmax = reinterpret_cast<uint32_t*>(X.inv_f + 8);
   auto full_bar = [&](int s) { return misc_a + 8u * s; };
   auto empty_bar = [&](int s) { return misc_a + 64u + 8u * s; };
-  auto xsum_bar = [&](int s) { return misc_a + 128u + 8u * s; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t x_bar = misc_a + 128u;   // x table landed (x-table variant)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.D; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), kConsumers + 1);
-      mbar_init(xsum_bar(s), 32);
+      mbar_init(empty_bar(s), C::WPT);   // one team consumes each stage
     }
+    mbar_init(x_bar, 1);
     *abort_flag = 0;
+    if constexpr (XT) {
+      for (int i = 0; i < 8; ++i) X.rmax[i] = 0u;
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -423,6 +774,15 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
       prefetch_tensormap(&tm_s);
       prefetch_tensormap(&tm_b);
       prefetch_tensormap(&tm_x);
+      if constexpr (XT) {
+        // the block's x, all K/64 groups of 8 rows, first of all
+        mbar_arrive_expect_tx(x_bar, (uint32_t)KG * 1024u);
+        if (p.x3d) {
+          tma_load_3d(X.lines, &tm_x, 0, 0, 0, x_bar);
+        } else {
+          for (int gi = 0; gi < KG; ++gi) tma_load_2d(X.lines + gi * 1024, &tm_x, gi * 64, 0, x_bar);
+        }
+      }
       int q = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
@@ -442,9 +802,15 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
           tma_load_2d(sb + kWeightBoxBytes, &tm_w, kt * (kBK / 8) + 32, rb * kBN, fb);
           tma_load_2d(sb + p.off_s, &tm_s, kt * (kBK / 64), rb * kBN, fb);
           tma_load_2d(sb + p.off_b, &tm_b, kt * (kBK / 64), rb * kBN, fb);
+          if constexpr (XT) {
+            // x comes from the block's table
+          } else if (p.x3d) {
+            tma_load_3d(sb + p.off_x, &tm_x, 0, 0, kt * kXBoxes, fb);
+          } else {
 #pragma unroll
-          for (int j = 0; j < kXBoxes; ++j)
-            tma_load_2d(sb + p.off_x + j * p.xbox_bytes, &tm_x, kt * kBK + j * kXBoxElems, 0, fb);
+            for (int j = 0; j < kXBoxes; ++j)
+              tma_load_2d(sb + p.off_x + j * MP * 128, &tm_x, kt * kBK + j * kXBoxElems, 0, fb);
+          }
           ++q;
         }
       }
@@ -457,29 +823,11 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
     return;
   }
 
-  if (warp == kHelperWarp) {
-    // ------------------------------------------------------------ helper
-    int q = 0;
-    for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-      const int sp = u - (u / p.S) * p.S;
-      const int kt0 = sp * p.KT / p.S, kt1 = (sp + 1) * p.KT / p.S;
-      for (int kt = kt0; kt < kt1; ++kt, ++q) {
-        const int slot = q % p.D;
-        const uint32_t ph = (uint32_t)(q / p.D) & 1u;
-        if (wait_or_abort(full_bar(slot), ph, abort_flag, p.err))
-          prepare_stage<ACT, MT>(sbase + slot * p.stage_bytes, p, lane);
-        mbar_arrive(xsum_bar(slot));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(slot));
-      }
-    }
-    return;
-  }
-
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, t = lane & 3;
-  const int rt = warp % kRowTiles, kh = warp / kRowTiles;
-  const int r0 = 16 * rt + 2 * g;
+  const int team = warp / C::WPT, wt = warp - (warp / C::WPT) * C::WPT;
+  const int rw = wt % RW, kq = wt / RW;
+  const int slice = team * KQ + kq;   // which partial sum of its rows this warp holds
   float best_v[MT][2];
   uint32_t best_n[MT][2];
   bool best_has[MT][2];
@@ -492,63 +840,114 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
       best_has[mt][c] = false;
     }
 
-  int q = 0;
   bool aborted = false;
+  // group sums of x (or the whole x table) for all of K, while the first
+  // stages are in flight
+  LaneOffsets<ACT, MT> lo;
+  XtLane xl;
+  uint32_t xsum_a = 0, T_a = 0, U_a = 0;
+  if constexpr (XT) {
+    if (!wait_or_abort(x_bar, 0u, abort_flag, p.err)) aborted = true;
+    build_xtab<ACT>(tabs, X, p, threadIdx.x, kConsumers * 32, kConsumers * 32);
+    xl = xt_lane<MT>(X.lines, rw, kq, g, t);
+    T_a = smem_addr(X.T) + xl.ts;
+    U_a = smem_addr(X.U) + xl.ts;
+  } else {
+    build_xsum<ACT, MT>(xsum, p, warp, lane, kConsumers);
+    named_bar_sync(1, kConsumers * 32);
+    lo = lane_offsets<ACT, MT>(rw, kq, g, t);
+    xsum_a = smem_addr(xsum) + lo.xs;
+  }
+
+  // stage counter q, and (slot, phase) of this team's next stage, advanced
+  // incrementally (no division in the loop)
+  int q = 0;
+  int slot = team, phase = 0;
+  while (slot >= p.D) {
+    slot -= p.D;
+    phase ^= 1;
+  }
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
     const int rb = u / p.S, sp = u - rb * p.S;
     const int kt0 = sp * p.KT / p.S, kt1 = (sp + 1) * p.KT / p.S;
-    float tot[MT][4];
+    float tot[RT][MT][4];
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) tot[mt][0] = tot[mt][1] = tot[mt][2] = tot[mt][3] = 0.f;
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) tot[r][mt][0] = tot[r][mt][1] = tot[r][mt][2] = tot[r][mt][3] = 0.f;
 
     for (int kt = kt0; kt < kt1; ++kt, ++q) {
-      const int slot = q % p.D;
-      const uint32_t ph = (uint32_t)(q / p.D) & 1u;
-      const bool ok = !aborted && wait_or_abort(full_bar(slot), ph, abort_flag, p.err) &&
-                      wait_or_abort(xsum_bar(slot), ph, abort_flag, p.err);
+      if (TEAMS > 1 && (q & (TEAMS - 1)) != team) continue;   // the other team's stage
+      const uint32_t ph = (uint32_t)phase;
+      const bool ok = !aborted && wait_or_abort(full_bar(slot), ph, abort_flag, p.err);
       if (ok) {
-        consume_stage<ACT, MT>(sbase + slot * p.stage_bytes, p, rt, kh, g, t, tot);
-        if constexpr (KH == 1)   // one warp per row tile covers both halves
-          consume_stage<ACT, MT>(sbase + slot * p.stage_bytes, p, rt, 1, g, t, tot);
+        if constexpr (XT)
+          consume_stage_xt<ACT>(base + slot * p.stage_bytes, kt, T_a, U_a, xl, tot);
+        else
+          consume_stage<ACT, MT>(base + slot * p.stage_bytes, xsum_a + kt * (8 * MP * 4), lo, tot);
       } else {
         aborted = true;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(slot));
+      slot += TEAMS;
+      if (slot >= p.D) {
+        slot -= p.D;
+        phase ^= 1;
+      }
     }
 
-    if constexpr (KH == 2) {
-      // add the second K-half into the first; red_k is [128 rows][MP]
-      if (kh == 1) {
+    if constexpr (SLICES > 1) {
+      // slices 1.. publish their partial sums, slice 0 adds them in order
+      if (slice > 0) {
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            red_k[(r0 + (e >> 1)) * MP + 8 * mt + 2 * t + (e & 1)] = tot[mt][e];
-      }
-      named_bar_sync(1, kConsumers * 32);
-      if (kh == 0) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            tot[mt][e] += red_k[(r0 + (e >> 1)) * MP + 8 * mt + 2 * t + (e & 1)];
-      }
-      named_bar_sync(1, kConsumers * 32);
-      if (kh == 1) continue;
-    }
-
-    const int n0 = rb * kBN + r0;   // this thread's rows n0 (e < 2) and n0 + 1
-    if constexpr (!ARGMAX) {
-      if (p.S == 1) {
-        if (!aborted) {
+        for (int r = 0; r < RT; ++r)
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const int n = n0 + (e >> 1), m = 8 * mt + 2 * t + (e & 1);
-              if (n < p.N && m < p.M) store_out<ACT>(p.y, (size_t)m * p.N + n, tot[mt][e]);
+              const int row = 16 * (RT * rw + r) + 2 * g + (e >> 1);
+              red_k[((slice - 1) * kBN + row) * MP + 8 * mt + 2 * t + (e & 1)] = tot[r][mt][e];
             }
+      }
+      named_bar_sync(1, kConsumers * 32);
+      if (slice == 0) {
+#pragma unroll
+        for (int k = 1; k < SLICES; ++k)
+#pragma unroll
+          for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int row = 16 * (RT * rw + r) + 2 * g + (e >> 1);
+                tot[r][mt][e] += red_k[((k - 1) * kBN + row) * MP + 8 * mt + 2 * t + (e & 1)];
+              }
+      }
+      named_bar_sync(1, kConsumers * 32);
+      if (slice > 0) continue;
+    }
+    if constexpr (XT) {
+      // back from the x table's per-row scale f_m to y
+#pragma unroll
+      for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) tot[r][0][e] *= X.inv_f[2 * t + (e & 1)];
+    }
+
+    if constexpr (!ARGMAX) {
+      if (p.S == 1) {
+        if (!aborted) {
+#pragma unroll
+          for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
+                const int m = 8 * mt + 2 * t + (e & 1);
+                if (n < p.N && m < p.M) store_out<ACT>(p.y, (size_t)m * p.N + n, tot[r][mt][e]);
+              }
         }
       } else {
         // split K: publish this slice, the last slice to arrive reduces all
@@ -556,12 +955,15 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
         float* part = p.part + (size_t)sp * p.M * p.N;
         if (!aborted) {
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
+          for (int r = 0; r < RT; ++r)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int n = n0 + (e >> 1), m = 8 * mt + 2 * t + (e & 1);
-              if (n < p.N && m < p.M) __stcg(part + (size_t)m * p.N + n, tot[mt][e]);
-            }
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
+                const int m = 8 * mt + 2 * t + (e & 1);
+                if (n < p.N && m < p.M) __stcg(part + (size_t)m * p.N + n, tot[r][mt][e]);
+              }
         }
         __threadfence();
         named_bar_sync(2, kEpiThreads);
@@ -571,17 +973,20 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
           __threadfence();
           if (!aborted) {
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+            for (int r = 0; r < RT; ++r)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int n = n0 + (e >> 1), m = 8 * mt + 2 * t + (e & 1);
-                if (n < p.N && m < p.M) {
-                  float s = 0.f;
-                  for (int k = 0; k < p.S; ++k)
-                    s += __ldcg(p.part + ((size_t)k * p.M + m) * p.N + n);
-                  store_out<ACT>(p.y, (size_t)m * p.N + n, s);
+              for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
+                  const int m = 8 * mt + 2 * t + (e & 1);
+                  if (n < p.N && m < p.M) {
+                    float s = 0.f;
+                    for (int k = 0; k < p.S; ++k)
+                      s += __ldcg(p.part + ((size_t)k * p.M + m) * p.N + n);
+                    store_out<ACT>(p.y, (size_t)m * p.N + n, s);
+                  }
                 }
-              }
           }
           if (threadIdx.x == 0) p.cnt[rb] = 0u;
         }
@@ -591,25 +996,27 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
       // running arg max per output row m over this thread's columns n
       // (n grows monotonically for a thread, so strict '>' keeps the lowest)
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
+      for (int r = 0; r < RT; ++r)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int n = n0 + (e >> 1), c = e & 1;
-          const float v = tot[mt][e] + 0.0f;   // -0 -> +0
-          if (!aborted && n < p.N && !(v != v)) {
-            if (!best_has[mt][c] || v > best_v[mt][c]) {
-              best_v[mt][c] = v;
-              best_n[mt][c] = (uint32_t)n;
-              best_has[mt][c] = true;
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1), c = e & 1;
+            const float v = tot[r][mt][e] + 0.0f;   // -0 -> +0
+            if (!aborted && n < p.N && !(v != v)) {
+              if (!best_has[mt][c] || v > best_v[mt][c]) {
+                best_v[mt][c] = v;
+                best_n[mt][c] = (uint32_t)n;
+                best_has[mt][c] = true;
+              }
             }
           }
-        }
     }
   }
 
   if constexpr (ARGMAX) {
-    if (KH == 2 && kh == 1) return;
-    // reduce over the 8 row-lanes g of the warp, then over the 8 row tiles
+    if (slice > 0) return;
+    // reduce over the 8 row-lanes g of the warp, then over the row warps
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -630,8 +1037,8 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
         }
         if (g == 0) {
           const int m = 8 * mt + 2 * t + c;
-          red_v[rt * 64 + m] = v;
-          red_i[rt * 64 + m] = h ? n : 0xFFFFFFFFu;
+          red_v[rw * 64 + m] = v;
+          red_i[rw * 64 + m] = h ? n : 0xFFFFFFFFu;
         }
       }
     named_bar_sync(2, kEpiThreads);
@@ -640,7 +1047,7 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
       float v = 0.f;
       uint32_t n = 0u;
       bool h = false;
-      for (int w = 0; w < kRowTiles; ++w) {
+      for (int w = 0; w < RW; ++w) {
         const uint32_t on = red_i[w * 64 + m];
         const float ov = red_v[w * 64 + m];
         if (better(ov, on, on != 0xFFFFFFFFu, v, n, h)) {
@@ -677,13 +1084,13 @@ __global__ void __launch_bounds__(threads_for(MT), 1)
   }
 }
 
-template <int ACT, int MT, bool AM>
+template <int ACT, int MT, bool AM, bool XT = false>
 int launch_one(const GemmLaunch& L) {
-  auto k = vq_gemm_kernel<ACT, MT, AM>;
+  auto k = vq_gemm_kernel<ACT, MT, AM, XT>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem) !=
       cudaSuccess)
     return VQ_ECUDA;
-  k<<<L.grid, threads_for(MT), L.smem, L.stream>>>(L.tm_w, L.tm_s, L.tm_b, L.tm_x, L.p);
+  k<<<L.grid, Cfg<MT>::THREADS, L.smem, L.stream>>>(L.tm_w, L.tm_s, L.tm_b, L.tm_x, L.p);
   return cudaGetLastError() == cudaSuccess ? VQ_OK : VQ_ECUDA;
 }
 
@@ -701,6 +1108,10 @@ int launch_gemm_act(const GemmLaunch& L) {
         return VQ_EUNSUPPORTED;
     }
   } else {
+    if (L.p.xt) {
+      if (L.MT != 1) return VQ_EUNSUPPORTED;
+      return L.argmax ? launch_one<ACT, 1, true, true>(L) : launch_one<ACT, 1, false, true>(L);
+    }
     switch (L.MT) {
       VQ_CASE(1)
       VQ_CASE(2)

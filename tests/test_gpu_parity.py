@@ -84,6 +84,34 @@ def test_linear_ragged_shapes(M, K, N, dtype):
     assert_proj_close(run_linear(x, w, dtype), oracle_linear(x, w, dtype), dtype)
 
 
+# wide N with M <= 8: several row blocks per block, so x is converted once
+# into a per-block fp16 table (the x-table variant)
+@pytest.mark.parametrize("M,K,N,dtype", [(8, 1024, 60000, "bf16"), (5, 512, 70001, "f16"),
+                                         (1, 2048, 58500, "bf16")])
+def test_linear_wide_n_x_table(M, K, N, dtype):
+    w = synth.w4_weights(M + K, N, K)
+    x = synth.activations(M + K, M, K, dtype)
+    y = run_linear(x, w, dtype)
+    cols = _sample_cols(N, 3, 300)
+    assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
+
+
+def test_linear_x_table_handles_large_and_tiny_rows():
+    # the per-row fp16 scaling keeps rows of very different magnitude exact
+    M, K, N = 4, 1024, 60000
+    w = synth.w4_weights(44, N, K)
+    base = np.random.default_rng(44).standard_normal((M, K)).astype(np.float32)
+    base[0] *= 3.0e4      # beyond fp16 range once multiplied by codes
+    base[1] *= 1.0e-6     # deep below fp16's normal range
+    base[2, ::7] = 0.0
+    x = synth.to_bf16_bits(base)
+    y = run_linear(x, w, "bf16")
+    cols = _sample_cols(N, 4, 200)
+    r = oracle_linear(x, w, "bf16", cols)
+    for m in range(M):
+        assert_proj_close(y[m:m + 1, cols], r[m:m + 1], "bf16")
+
+
 @pytest.mark.parametrize("M,K,N", [(8, 5120, 1024), (4, 4096, 256), (16, 2560, 640)])
 def test_linear_split_k_is_exact_and_repeatable(M, K, N):
     w = synth.w4_weights(11, N, K)
@@ -127,19 +155,23 @@ def test_linear_block_size_and_dtype_sweep(sweep_weights, M, dtype):
 
 
 def test_rows_are_independent_and_permute():
-    # a row's result does not depend on the other rows of the block (so M=1,
-    # the M=8 block and the M=16 block agree bit for bit), and permuting the
+    # a row's result does not depend on the other rows of the block: M=1 and
+    # the M=8 block agree bit for bit (same code path), the M=16 block agrees
+    # within the tolerance (its rows take the general path), and permuting the
     # rows permutes the output
     w = synth.w4_weights(21, 700, 1024)
     x16 = synth.activations(21, 16, 1024, "bf16")
     y16 = run_linear(x16, w, "bf16")
     y8 = run_linear(x16[:8].copy(), w, "bf16")
     y1 = run_linear(x16[5:6].copy(), w, "bf16")
-    assert np.array_equal(y16[:8], y8)
-    assert np.array_equal(y16[5], y1[0])
-    perm = np.random.default_rng(0).permutation(16)
-    yp = run_linear(x16[perm].copy(), w, "bf16")
-    assert np.array_equal(yp, y16[perm])
+    assert np.array_equal(y8[5], y1[0])
+    r8 = oracle_linear(x16[:8].copy(), w, "bf16")
+    assert_proj_close(y8, r8, "bf16")
+    assert_proj_close(y16[:8], r8, "bf16")
+    for M, xs, ys in ((16, x16, y16), (8, x16[:8].copy(), y8)):
+        perm = np.random.default_rng(M).permutation(M)
+        yp = run_linear(xs[perm].copy(), w, "bf16")
+        assert np.array_equal(yp, ys[perm])
 
 
 def test_linear_paper_shape_is_deterministic():
@@ -203,7 +235,7 @@ def test_vocab_argmax_exact_tie_takes_lowest_index():
 
 
 @pytest.mark.parametrize("M,K,N", [(3, 512, 1000), (16, 1024, 5000), (64, 512, 2049),
-                                   (33, 1536, 777)])
+                                   (33, 1536, 777), (8, 512, 60000), (2, 1024, 77777)])
 def test_vocab_argmax_ragged(M, K, N):
     w = synth.w4_weights(M + N, N, K)
     x = synth.activations(M + N, M, K, "bf16")
