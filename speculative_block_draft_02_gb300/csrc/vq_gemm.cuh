@@ -107,7 +107,7 @@ __host__ __device__ constexpr int xt_stage_off_s() { return 2 * kWeightBoxBytes;
 __host__ __device__ constexpr int xt_stage_bytes() {
   return (xt_stage_off_s() + 2 * kBN * 16 + 1023) / 1024 * 1024;
 }
-// x table [K/64 groups][8 rows][128 B] fp16 + T and U tables [K/64][8] fp32 +
+// x table [K/64 groups][8 rows][128 B] fp16 + T and scratch tables [K/64][8] fp32 +
 // per-row 1/f [8] fp32 + per-row max bits [8] u32.
 __host__ __device__ constexpr int xt_table_bytes(int K) { return (K / 64) * 1024 + 2 * (K / 64) * 32 + 64; }
 constexpr int kMaxXtBytes = 96 * 1024;
@@ -522,16 +522,15 @@ __device__ __forceinline__ void build_xsum(float* xsum, const GemmParams& p, int
 //   phi_i = 1 for even i and 1/16 for odd i, and f_m = 2^(13 - floor(log2
 //   max|x_m|)) so that every |x'| < 2^14 (no fp16 overflow, whatever the
 //   scale of the activations).
-// With codes entered as the fp16 values 1024 + q (even i) and 1024 + 16q (odd
-// i), taken straight from nibble positions 0-3 and 4-7 of each byte pair,
-// each MMA product is (1024 + q) x' or (1024 + 16q) x'/16 scaled by f_m, so
-//   acc_g = f_m * sum_g q x + U_g,  U_g = 1024 * sum_g x'
-// and the group folds as  tot += s * (acc_g - U_g) + b * T_g,  T_g = f_m * sum_g x,
+// Codes enter the MMA as the exact fp16 values q (even i) and 16q (odd i),
+// taken from nibble positions 0-3 and 4-7 of each byte pair (one AND/OR with
+// the pattern of 1024.0 and one fp16 subtraction), so each product is q x'
+// and the group folds as  tot += s * acc_g + b * T_g,  T_g = f_m * sum_g x,
 // with y = tot / f_m at the end.
 struct XTab {
   uint32_t lines;   // shared address of the fp16 table
-  float* T;         // [K/64][8]
-  float* U;         // [K/64][8]
+  float* T;         // [K/64][8] group sums f_m * sum x
+  float* U;         // [K/64][8] scratch of the table build
   float* inv_f;     // [8]
   uint32_t* rmax;   // [8] float bits of max |x_m|
 };
@@ -588,7 +587,7 @@ __device__ __forceinline__ void build_xtab(uint8_t* tab_gen, const XTab& X, cons
     }
   }
   named_bar_sync(1, bar_threads);
-  // pass B: scale and convert in place; turn the sums into T and U
+  // pass B: scale and convert in place; turn the sums into T
   for (int ci = tid; ci < chunks; ci += n_threads) {
     const int m = (ci >> 3) & 7, gi = ci >> 6, c = ci & 7;
     const float f = row_scale(X.rmax[m]);
@@ -605,7 +604,6 @@ __device__ __forceinline__ void build_xtab(uint8_t* tab_gen, const XTab& X, cons
     if (c == 0) {
       const float se = X.T[gi * 8 + m], so = X.U[gi * 8 + m];
       X.T[gi * 8 + m] = f * (se + so);
-      X.U[gi * 8 + m] = 1024.f * f * (se + 0.0625f * so);
     }
   }
   if (tid < 8) X.inv_f[tid] = 1.f / row_scale(X.rmax[tid]);
@@ -638,16 +636,25 @@ __device__ __forceinline__ XtLane xt_lane(uint32_t lines, int rw, int kq, int g,
   return o;
 }
 
+// Nibbles of a word under `mask` (bits 0-3 or 4-7 of each 16-bit half) as an
+// exact fp16 pair: q, or 16q for the upper nibble position.
+__device__ __forceinline__ uint32_t xt_code(uint32_t w, uint32_t mask) {
+  constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0 in both halves
+  const uint32_t v = lop3_and_or(w, mask, kMagic);
+  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&v),
+                            *reinterpret_cast<const __half2*>(&kMagic));
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // One stage of the x-table variant (MT = 1): groups kq*GPW .. +GPW-1 of
 // stage kt for the warp's RT row tiles.
 template <int ACT>
-__device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T_a, uint32_t U_a,
+__device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T_a,
                                                  const XtLane& o,
                                                  float (&tot)[Cfg<1>::RT][1][4]) {
   using C = Cfg<1>;
   constexpr int RT = C::RT, GPW = C::GPW;
   constexpr int kBiasOff = kBN * 16;
-  constexpr uint32_t kMagic = 0x64006400u;   // fp16 1024.0 in both halves
   static_assert(GPW == 4 || GPW == 8, "K-slices of 4 or 8 groups");
 
   Packed<GPW> sc0[RT], sc1[RT], bi0[RT], bi1[RT];
@@ -662,7 +669,7 @@ __device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T
   const uint32_t we = sb + o.w_even, wo = sb + o.w_odd;
   const uint32_t xg = (uint32_t)kt * 8 * 1024;   // the stage's first group in the x table
   const uint32_t xa0 = o.x_h0 + xg, xa1 = o.x_h1 + xg;
-  const uint32_t ta = T_a + (uint32_t)kt * 8 * 32, ua = U_a + (uint32_t)kt * 8 * 32;
+  const uint32_t ta = T_a + (uint32_t)kt * 8 * 32;
 
   static_for<GPW>([&](auto jc) {
     constexpr int jj = decltype(jc)::value;
@@ -684,11 +691,12 @@ __device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T
         const uint32_t qa = h ? wa[r].y : wa[r].x;
         const uint32_t qb = h ? wb[r].y : wb[r].x;
         const uint32_t qa8 = qa >> 8, qb8 = qb >> 8;
-        // step s' = 0: pairs (c0,c4) and (c1,c5); s' = 1: (c2,c6) and (c3,c7)
-        const uint32_t a0[4] = {lop3_and_or(qa, 0x000F000Fu, kMagic), lop3_and_or(qb, 0x000F000Fu, kMagic),
-                                lop3_and_or(qa, 0x00F000F0u, kMagic), lop3_and_or(qb, 0x00F000F0u, kMagic)};
-        const uint32_t a1[4] = {lop3_and_or(qa8, 0x000F000Fu, kMagic), lop3_and_or(qb8, 0x000F000Fu, kMagic),
-                                lop3_and_or(qa8, 0x00F000F0u, kMagic), lop3_and_or(qb8, 0x00F000F0u, kMagic)};
+        // step s' = 0: pairs (c0,c4) and (c1,c5); s' = 1: (c2,c6) and (c3,c7);
+        // made exact (q or 16q) by one fp16 subtraction on the FMA pipe
+        const uint32_t a0[4] = {xt_code(qa, 0x000F000Fu), xt_code(qb, 0x000F000Fu),
+                                xt_code(qa, 0x00F000F0u), xt_code(qb, 0x00F000F0u)};
+        const uint32_t a1[4] = {xt_code(qa8, 0x000F000Fu), xt_code(qb8, 0x000F000Fu),
+                                xt_code(qa8, 0x00F000F0u), xt_code(qb8, 0x00F000F0u)};
         float (&d)[4] = acc[r];
         if (h == 0)
           mma_16816_zc<true>(d, a0, bx.x, bx.y);
@@ -697,18 +705,17 @@ __device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T
         mma_16816<true>(d, a1, bx.z, bx.w);
       }
     });
-    // fold: tot += s * (acc - U) + b * T, rows 2t and 2t+1 of the block
-    const uint2 tv = lds64<jj * 32>(ta), uv = lds64<jj * 32>(ua);
+    // fold: tot += s * acc + b * T, rows 2t and 2t+1 of the block
+    const uint2 tv = lds64<jj * 32>(ta);
     const float T0 = __uint_as_float(tv.x), T1 = __uint_as_float(tv.y);
-    const float U0 = __uint_as_float(uv.x), U1 = __uint_as_float(uv.y);
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
       const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
       const float b_a = bf16_of(bi0[r], jj), b_b = bf16_of(bi1[r], jj);
-      tot[r][0][0] = fmaf(s_a, acc[r][0], fmaf(b_a, T0, fmaf(-s_a, U0, tot[r][0][0])));
-      tot[r][0][1] = fmaf(s_a, acc[r][1], fmaf(b_a, T1, fmaf(-s_a, U1, tot[r][0][1])));
-      tot[r][0][2] = fmaf(s_b, acc[r][2], fmaf(b_b, T0, fmaf(-s_b, U0, tot[r][0][2])));
-      tot[r][0][3] = fmaf(s_b, acc[r][3], fmaf(b_b, T1, fmaf(-s_b, U1, tot[r][0][3])));
+      tot[r][0][0] = fmaf(s_a, acc[r][0], fmaf(b_a, T0, tot[r][0][0]));
+      tot[r][0][1] = fmaf(s_a, acc[r][1], fmaf(b_a, T1, tot[r][0][1]));
+      tot[r][0][2] = fmaf(s_b, acc[r][2], fmaf(b_b, T0, tot[r][0][2]));
+      tot[r][0][3] = fmaf(s_b, acc[r][3], fmaf(b_b, T1, tot[r][0][3]));
     }
   });
 }
@@ -845,13 +852,12 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   // stages are in flight
   LaneOffsets<ACT, MT> lo;
   XtLane xl;
-  uint32_t xsum_a = 0, T_a = 0, U_a = 0;
+  uint32_t xsum_a = 0, T_a = 0;
   if constexpr (XT) {
     if (!wait_or_abort(x_bar, 0u, abort_flag, p.err)) aborted = true;
     build_xtab<ACT>(tabs, X, p, threadIdx.x, kConsumers * 32, kConsumers * 32);
     xl = xt_lane<MT>(X.lines, rw, kq, g, t);
     T_a = smem_addr(X.T) + xl.ts;
-    U_a = smem_addr(X.U) + xl.ts;
   } else {
     build_xsum<ACT, MT>(xsum, p, warp, lane, kConsumers);
     named_bar_sync(1, kConsumers * 32);
@@ -882,7 +888,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       const bool ok = !aborted && wait_or_abort(full_bar(slot), ph, abort_flag, p.err);
       if (ok) {
         if constexpr (XT)
-          consume_stage_xt<ACT>(base + slot * p.stage_bytes, kt, T_a, U_a, xl, tot);
+          consume_stage_xt<ACT>(base + slot * p.stage_bytes, kt, T_a, xl, tot);
         else
           consume_stage<ACT, MT>(base + slot * p.stage_bytes, xsum_a + kt * (8 * MP * 4), lo, tot);
       } else {
