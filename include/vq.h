@@ -112,6 +112,29 @@ int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_t* qw,
                     void* stream);
 
 /*
+ * vq_vocab_argmax without a workspace: the same operation, arguments and
+ * results as vq_vocab_argmax, but its scratch memory (M*8 + 4 bytes, rounded
+ * up to 16) lives in a fixed 1 KiB array inside this library, so the call
+ * allocates nothing. The pages have no counterpart of this entry point; it is
+ * there for callers that cannot call cudaMalloc or have a buffer made for
+ * them: serving runtimes that forbid device allocation once they are running
+ * (an allocation can block, fragment memory or fail at a bad moment), and
+ * plug-ins embedded in a host application that owns all device memory and
+ * hands out none for scratch.
+ *
+ * Limit: 1 <= M <= 64 (the array's size); a larger M returns VQ_EINVAL.
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address; make that first call before any stream capture.
+ * The array is held by every GPU that loads the library until the process
+ * exits. Each call clears the part it uses on `stream` before the kernel.
+ * Calls share the one array: calls that can overlap on the GPU (different
+ * streams, or different host threads) race and must not be made.
+ */
+int vq_vocab_argmax_noalloc(const void* x, int M, int K, int N, const uint32_t* qw,
+                            const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                            int32_t* argmax, float* maxval, void* stream);
+
+/*
  * Per-row accept walk.
  *
  * Source: mlxcel #2865 "perf(speculative): commit per-row accepts in batched

@@ -27,6 +27,7 @@ SIGNATURES = {
     "vq_linear": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _P, _S, _P]),
     "vq_vocab_argmax_workspace_bytes": (_S, [_I]),
     "vq_vocab_argmax": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _S, _P]),
+    "vq_vocab_argmax_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
     "verify_accept_walk": (_I, [_P, _P, _I, _I, _P, _P]),
     "kv_compact_per_row": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
     "vq_strerror": (ctypes.c_char_p, [_I]),
@@ -109,6 +110,18 @@ def vq_vocab_argmax(x, qw, scales, biases, workspace, argmax=None, maxval=None, 
                                _ACT[x.dtype], _ptr(argmax), _ptr(maxval), _ptr(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "vq_vocab_argmax")
+    return argmax, maxval
+
+
+def vq_vocab_argmax_noalloc(x, qw, scales, biases, argmax=None, maxval=None, stream=None):
+    """vq_vocab_argmax with the library's own fixed scratch instead of a workspace."""
+    M, K = x.shape
+    N = qw.shape[0]
+    if argmax is None:
+        argmax = torch.empty(M, dtype=torch.int32, device=x.device)
+    rc = lib().vq_vocab_argmax_noalloc(_ptr(x), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
+                                       _ACT[x.dtype], _ptr(argmax), _ptr(maxval), _stream(stream))
+    _check(rc, "vq_vocab_argmax_noalloc")
     return argmax, maxval
 
 

@@ -318,6 +318,50 @@ extern "C" int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_
                   workspace, workspace_bytes, stream);
 }
 
+// ---------------------------------------------------------------- no-alloc arg max
+// Scratch of vq_vocab_argmax_noalloc: one file-scope device array instead of
+// a caller-provided workspace. It holds the arg max workspace of every valid
+// M (M * 8 + 4 bytes rounded up to 16, at most 528 bytes for M = 64). Every
+// GPU that loads this library holds it until the process exits, and every
+// call on that GPU shares it.
+namespace vq {
+namespace {
+constexpr size_t kNoAllocScratchBytes = 1024;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_ptr[kMaxDevices];   // device address of the array, per device
+}  // namespace
+}  // namespace vq
+
+extern "C" int vq_vocab_argmax_noalloc(const void* x, int M, int K, int N, const uint32_t* qw,
+                                       const uint16_t* scales, const uint16_t* biases,
+                                       int act_dtype, int32_t* argmax, float* maxval,
+                                       void* stream) {
+  if (M < 1 || M > 64) return VQ_EINVAL;
+  const size_t need = vq_vocab_argmax_workspace_bytes(M);
+  if (need == 0 || need > kNoAllocScratchBytes) return VQ_EWORKSPACE;
+  int dev;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  void* scratch;
+  {
+    // set-up, once per device with that device current: the host-side name
+    // of the array is not a device address, so look the address up
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return VQ_ECUDA;
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  // the array keeps whatever the last call left: clear the keys and the
+  // block counter, which must start at zero, on the call's stream
+  if (cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return VQ_ECUDA;
+  return run_gemm(x, M, K, N, qw, scales, biases, act_dtype, true, nullptr, argmax, maxval,
+                  scratch, need, stream);
+}
+
 extern "C" const char* vq_strerror(int code) {
   switch (code) {
     case VQ_OK:
