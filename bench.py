@@ -224,6 +224,17 @@ def dev_act(seed, M_, K_, dtype="bf16", scale=1.0, name="x"):
     return xb, torch.from_numpy(xb.view(np.int16).copy()).view(tdt).cuda()
 
 
+def launches_per_call(vq, M_, K_, N_):
+    # 16-bit x with M <= 8 and a workspace for the prepared x table: the table
+    # kernel, then the projection
+    return 2 if vq.vq_linear_workspace_bytes(M_, K_, N_, torch.bfloat16) >= 16 * K_ else 1
+
+
+def workspace_for(vq, M_, K_, N_, dt):
+    nb = vq.vq_linear_workspace_bytes(M_, K_, N_, dt)
+    return torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
+
+
 def n_copies_for(bytes_per_copy):
     return max(2, -(-4 * L2_BYTES // bytes_per_copy))
 
@@ -280,8 +291,8 @@ def run_ours(args):
     w, copies = dev_weights(0, n_cp, N, K)
     xb, x = dev_act(0, M, K)
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    assert vq.vq_linear_workspace_bytes(M, K, N) == 0
-    calls = [(lambda c=c: vq.vq_linear(x, *c, y=y)) for c in copies]
+    ws = workspace_for(vq, M, K, N, torch.bfloat16)
+    calls = [(lambda c=c: vq.vq_linear(x, *c, y=y, workspace=ws)) for c in copies]
 
     clocks = ClockSampler(dev)
     total, per_launch = time_calls(calls, K_steps, W, world)
@@ -300,7 +311,7 @@ def run_ours(args):
     e2e_steps = K_steps
     for i in range(W):
         x_dev.copy_(x_host, non_blocking=True)
-        vq.vq_linear(x_dev, *copies[i % n_cp], y=y)
+        vq.vq_linear(x_dev, *copies[i % n_cp], y=y, workspace=ws)
         y_host.copy_(y, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     barrier(world)
@@ -308,7 +319,7 @@ def run_ours(args):
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         x_dev.copy_(x_host, non_blocking=True)
-        vq.vq_linear(x_dev, *copies[i % n_cp], y=y)
+        vq.vq_linear(x_dev, *copies[i % n_cp], y=y, workspace=ws)
         y_host.copy_(y, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
@@ -333,7 +344,7 @@ def run_ours(args):
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes": b_main, "kernel": "vq_gemm_kernel<bf16,MT=1>",
                      "us_per_launch": per_launch * 1e6},
-        "e2e": e2e, "gpu_launches": K_steps, "clocks": clk,
+        "e2e": e2e, "gpu_launches": K_steps * launches_per_call(vq, M, K, N), "clocks": clk,
     }
 
     if not args.no_path:
@@ -368,8 +379,7 @@ def path_table(vq, copies, x, W, world):
     for Mi in (4, 8):
         _, xi = dev_act(0, Mi, K, "bf16", 0.5)
         yi = torch.empty((Mi, 1024), dtype=torch.bfloat16, device="cuda")
-        wsi = torch.zeros(max(vq.vq_linear_workspace_bytes(Mi, K, 1024), 16), dtype=torch.uint8,
-                          device="cuda")
+        wsi = workspace_for(vq, Mi, K, 1024, torch.bfloat16)
         record("verify_m%d_k5120_n1024_bf16" % Mi,
                [(lambda c=c, xi=xi, yi=yi, wsi=wsi: vq.vq_linear(xi, *c, y=yi, workspace=wsi))
                 for c in c1], alg_bytes(Mi, K, 1024), rows=Mi)
@@ -380,9 +390,11 @@ def path_table(vq, copies, x, W, world):
         for Mi in (1, 4, 8, 16):
             _, xi = dev_act(0, Mi, K, dt, 0.5)
             yi = torch.empty((Mi, N), dtype=xi.dtype, device="cuda")
+            wsi = workspace_for(vq, Mi, K, N, xi.dtype)
             eb = 4 if dt == "f32" else 2
             record("verify_m%d_k5120_n17408_%s" % (Mi, dt),
-                   [(lambda c=c, xi=xi, yi=yi: vq.vq_linear(xi, *c, y=yi)) for c in copies],
+                   [(lambda c=c, xi=xi, yi=yi, wsi=wsi: vq.vq_linear(xi, *c, y=yi, workspace=wsi))
+                    for c in copies],
                    alg_bytes(Mi, K, N, eb, eb), rows=Mi)
         out["ratio_m8_over_m4_rows_n17408_%s" % dt] = (
             out["verify_m8_k5120_n17408_%s" % dt]["rows_per_s"] /
@@ -391,8 +403,10 @@ def path_table(vq, copies, x, W, world):
     # next-block verify at M=64 (B=4 x block 16)
     _, x64 = dev_act(0, 64, K, "bf16", name="x_next")
     y64 = torch.empty((64, N), dtype=torch.bfloat16, device="cuda")
+    ws64 = workspace_for(vq, 64, K, N, torch.bfloat16)
     record("verify_m64_k5120_n17408_bf16",
-           [(lambda c=c: vq.vq_linear(x64, *c, y=y64)) for c in copies], alg_bytes(64, K, N),
+           [(lambda c=c: vq.vq_linear(x64, *c, y=y64, workspace=ws64)) for c in copies],
+           alg_bytes(64, K, N),
            rows=64, n=100)
 
     # vocab projection + fused arg max, M=64, K=2560, N=151936

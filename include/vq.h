@@ -24,6 +24,15 @@
  *   - Row-major layouts throughout; sizes are in elements unless noted.
  *   - A workspace may be shared by successive calls on one stream, never by
  *     calls that can run at the same time.
+ *   - vq_linear, vq_vocab_argmax and vq_vocab_argmax_noalloc launch their
+ *     kernels with programmatic stream serialization, so that back-to-back
+ *     projections overlap: a kernel may start while the kernel before it in
+ *     the stream is finishing. It requests its first weight stages (qw,
+ *     scales, biases) right away, and reads x and writes its outputs and
+ *     workspace only after that kernel has completed (griddepcontrol.wait).
+ *     So the weights must not be written by the kernel launched immediately
+ *     before the call on the same stream; weights written at load time are
+ *     fine, as is any write followed by another operation on the stream.
  */
 #ifndef VQ_H_
 #define VQ_H_
@@ -69,11 +78,16 @@ extern "C" {
  * y        [M][N] output in act_dtype (round to nearest even from the fp32
  *          accumulator; fp32 output for VQ_F32), 4-byte aligned.
  * workspace / workspace_bytes
- *          scratch for the split-K reduction used when N is too narrow to fill
- *          the GPU. vq_linear_workspace_bytes() gives the size needed (0 when
- *          no split is used; then workspace may be NULL). The workspace must
- *          be zero-filled before its first use; every call leaves it
- *          zero-filled again. 16-byte aligned.
+ *          scratch for (a) x converted once per call into per-stage slices of
+ *          scaled fp16 MMA fragments (16-bit x with M <= 8: about 17.6*K
+ *          bytes), and (b) the split-K reduction used when N is too narrow to
+ *          fill the GPU. vq_linear_workspace_bytes() gives the size needed (0
+ *          when neither is used; then workspace may be NULL). The workspace
+ *          must be zero-filled before its first use; every call leaves the
+ *          part that must start at zero zero-filled again. 16-byte aligned.
+ *          With the slices, the call enqueues two kernels: the slices, then
+ *          the projection, which may start before the slices are done and
+ *          waits for them.
  * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 512,
  *          N >= 1. Other K (multiples of 64) return VQ_EUNSUPPORTED.
  * Accumulation is fp32; each 64-wide group is accumulated from exact integer

@@ -104,10 +104,12 @@ int red_bytes(int MT) {
 
 // Shape of one launch: everything but the pointers.
 struct Plan {
-  int MT, MP, D, KT, RB, S, n_units, grid;
-  int stage_bytes, off_x, off_s, off_b, xbox_bytes, xt, tab_bytes;
+  int MT, MP, D, pre, KT, RB, S, n_units, grid;
+  bool red_alias;   // K-slice partials in the stage ring (one unit per block)
+  int stage_bytes, off_x, off_s, off_b, xbox_bytes, xm, tab_bytes;
   uint32_t tx_bytes;
   size_t smem;
+  size_t ws_xp_bytes;    // prepared x table (start of the workspace), 0 if none
   size_t ws_cnt_bytes, ws_bytes;
 };
 
@@ -127,39 +129,15 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   p.MP = 8 * p.MT;
   const bool f32 = act == VQ_F32;
   const int n_xbox = f32 ? 16 : 8;
-  // x for the stage: [group][8*MT rows][128 B]; rows >= M are zero-filled.
-  // For 16-bit x with M <= 8 whose fp16 table fits, x is converted once per
-  // block instead (the x-table variant) and the stages carry weights only.
-  const int red = red_bytes(p.MT);
-  // (the conversion costs about as much as two row blocks of the main loop
-  // save, so it is used only when a block processes several row blocks)
-  const long long rb_total = ((long long)N + kBN - 1) / kBN;
-  const long long per_block = argmax ? (rb_total + sms - 1) / sms : (rb_total >= sms ? (rb_total + sms - 1) / sms : 1);
-  p.xt = (!f32 && p.MT == 1 && xt_table_bytes(K) <= kMaxXtBytes && per_block >= 3) ? 1 : 0;
-  int tab;
-  if (p.xt) {
-    p.xbox_bytes = 0;
-    p.off_x = 0;
-    p.off_s = xt_stage_off_s();
-    p.off_b = xt_stage_off_s() + kBN * 16;
-    p.stage_bytes = xt_stage_bytes();
-    tab = xt_table_bytes(K);
-  } else {
-    p.xbox_bytes = 128 * p.MP;
-    p.off_x = stage_off_x();
-    p.off_s = stage_off_s(act, p.MT);
-    p.off_b = stage_off_b(act, p.MT);
-    p.stage_bytes = stage_bytes(act, p.MT);
-    tab = xsum_bytes(K, p.MT);
-    if (tab > kMaxXsumBytes) return VQ_EUNSUPPORTED;
-  }
-  tab = (int)round_up((size_t)tab, 1024);
-  p.D = (kSmemLimit - 1024 - kMiscBytes - red - tab) / p.stage_bytes;
-  if (p.D > kMaxStages) p.D = kMaxStages;
-  if (p.D < 2) return VQ_EUNSUPPORTED;
-  p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + (size_t)n_xbox * p.xbox_bytes);
-  p.tab_bytes = tab;
-  p.smem = 1024 + (size_t)p.D * p.stage_bytes + kMiscBytes + red + tab;
+  // Where x comes from:
+  //  xm = 2 (vq_linear, 16-bit x, M <= 8): slices of scaled fp16 fragments
+  //         prepared by a small kernel before the projection, one per stage,
+  //         copied into the stage next to its weights;
+  //  xm = 1 (arg max, 16-bit x, M <= 8, several row blocks per block): the
+  //         block converts all of x once into a table (the conversion costs
+  //         about what two row blocks of the main loop save);
+  //  xm = 0 otherwise: x for the stage by TMA, [group][8*MT rows][128 B] with
+  //         rows >= M zero-filled, and a table of group sums per block.
   p.KT = K / kBK;
   p.RB = (int)(((long long)N + kBN - 1) / kBN);
   p.S = 1;
@@ -174,14 +152,70 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   }
   p.n_units = p.RB * p.S;
   p.grid = p.n_units < sms ? p.n_units : sms;
+  // The K-slice partial sums are only needed after a unit's last stage: with
+  // one unit per block they can share the stage ring instead of taking
+  // shared memory of their own.
+  p.red_alias = p.n_units <= p.grid && red_bytes(p.MT) > 0;
+  const int red = p.red_alias ? 0 : red_bytes(p.MT);
+  const long long rb_total = ((long long)N + kBN - 1) / kBN;
+  const long long per_block = (rb_total + sms - 1) / sms;
+  const bool mt1_16 = !f32 && p.MT == 1;
+  if (mt1_16 && !argmax)
+    p.xm = 2;
+  else if (mt1_16 && argmax && xt_table_bytes(K) <= kMaxXtBytes && per_block >= 3)
+    p.xm = 1;
+  else
+    p.xm = 0;
+  p.ws_xp_bytes = (p.xm == 2) ? round_up((size_t)(K / kBK) * kSliceBytes, 256) : 0;
+  int tab;
+  int x_bytes;   // x bytes a stage receives
+  if (p.xm == 2) {
+    p.xbox_bytes = 0;
+    p.off_x = xs_stage_off_x();
+    p.off_s = xt_stage_off_s();
+    p.off_b = xt_stage_off_s() + kBN * 16;
+    p.stage_bytes = xs_stage_bytes();
+    tab = 0;
+    x_bytes = kSliceBytes;
+  } else if (p.xm == 1) {
+    p.xbox_bytes = 0;
+    p.off_x = 0;
+    p.off_s = xt_stage_off_s();
+    p.off_b = xt_stage_off_s() + kBN * 16;
+    p.stage_bytes = xt_stage_bytes();
+    tab = xt_table_bytes(K);
+    x_bytes = 0;
+  } else {
+    p.xbox_bytes = 128 * p.MP;
+    p.off_x = stage_off_x();
+    p.off_s = stage_off_s(act, p.MT);
+    p.off_b = stage_off_b(act, p.MT);
+    p.stage_bytes = stage_bytes(act, p.MT);
+    tab = xsum_bytes(K, p.MT);
+    if (tab > kMaxXsumBytes) return VQ_EUNSUPPORTED;
+    x_bytes = n_xbox * p.xbox_bytes;
+  }
+  tab = (int)round_up((size_t)tab, 1024);
+  p.D = (kSmemLimit - 1024 - misc_bytes(argmax) - red - tab) / p.stage_bytes;
+  if (p.D > kMaxStages) p.D = kMaxStages;
+  if (p.D < 2) return VQ_EUNSUPPORTED;
+  // stages whose weights a block requests before it waits for the kernel
+  // before it in the stream. Three measured best for the projection: the
+  // first stages' x then queues behind fewer weight bytes.
+  p.pre = p.D < 3 ? p.D : 3;
+  p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + x_bytes);
+  p.tab_bytes = tab;
+  p.smem = 1024 + (size_t)p.D * p.stage_bytes + misc_bytes(argmax) + red + tab;
+  // workspace: [prepared x table][split-K counters][split-K partials]
   if (argmax) {
     p.ws_cnt_bytes = 0;
     p.ws_bytes = round_up((size_t)M * 8 + 4, 16);
   } else if (p.S > 1) {
     p.ws_cnt_bytes = round_up((size_t)p.RB * 4, 16);
-    p.ws_bytes = p.ws_cnt_bytes + (size_t)p.S * M * N * 4;
+    p.ws_bytes = p.ws_xp_bytes + p.ws_cnt_bytes + (size_t)p.S * M * N * 4;
   } else {
-    p.ws_cnt_bytes = p.ws_bytes = 0;
+    p.ws_cnt_bytes = 0;
+    p.ws_bytes = p.ws_xp_bytes;
   }
   *pl = p;
   return VQ_OK;
@@ -218,13 +252,15 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
   p.S = pl.S;
   p.n_units = pl.n_units;
   p.D = pl.D;
+  p.pre = pl.pre;
+  p.red_alias = pl.red_alias ? 1 : 0;
   p.stage_bytes = pl.stage_bytes;
   p.off_x = pl.off_x;
   p.off_s = pl.off_s;
   p.off_b = pl.off_b;
 
   p.tx_bytes = pl.tx_bytes;
-  p.xt = pl.xt;
+  p.xm = pl.xm;
   p.tab_bytes = pl.tab_bytes;
   p.y = y;
   p.err = err;
@@ -233,9 +269,12 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
     p.done = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + (size_t)M * 8);
     p.argmax = amax;
     p.maxval = maxval;
-  } else if (pl.S > 1) {
-    p.cnt = static_cast<uint32_t*>(ws);
-    p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_cnt_bytes);
+  } else {
+    if (pl.ws_xp_bytes) p.xprep = ws;
+    if (pl.S > 1) {
+      p.cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + pl.ws_xp_bytes);
+      p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_xp_bytes + pl.ws_cnt_bytes);
+    }
   }
 
   const bool f32 = act == VQ_F32;
@@ -257,7 +296,7 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
   const int eb = f32 ? 4 : 2;
   // box rows = 8*MT >= M: the rows past M are out of range and arrive zeroed;
   // the x-table variant takes every group of K in one box
-  if (encode_x3d(&L.tm_x, xdt, x, M, K, eb, pl.MP, pl.xt ? K / 64 : kBK / (128 / eb)) == VQ_OK) {
+  if (encode_x3d(&L.tm_x, xdt, x, M, K, eb, pl.MP, pl.xm == 1 ? K / 64 : kBK / (128 / eb)) == VQ_OK) {
     p.x3d = 1;
   } else {
     if ((rc = encode_2d(&L.tm_x, xdt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * eb, 128 / eb,

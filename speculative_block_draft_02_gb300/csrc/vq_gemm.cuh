@@ -67,6 +67,8 @@ constexpr int kWeightBoxBytes = kBN * 128;   // 128 rows x 32 words
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per block
 // misc area after the stage ring: 2 x 8 mbarriers, flags, arg max scratch
 constexpr int kMiscBytes = 256 + 2 * 8 * 64 * 4;
+// bytes of the misc region: the arg max's cross-warp buffers only with ARGMAX
+__host__ __device__ constexpr int misc_bytes(bool argmax) { return argmax ? kMiscBytes : 256; }
 
 // Work split of the consumers by the number MT of n8 tiles (M <= 8*MT):
 // TEAMS teams taking alternate stages, RT 16-row tiles per warp (two tiles
@@ -107,9 +109,26 @@ __host__ __device__ constexpr int xt_stage_off_s() { return 2 * kWeightBoxBytes;
 __host__ __device__ constexpr int xt_stage_bytes() {
   return (xt_stage_off_s() + 2 * kBN * 16 + 1023) / 1024 * 1024;
 }
-// x table [K/64 groups][8 rows][128 B] fp16 + T and scratch tables [K/64][8] fp32 +
-// per-row 1/f [8] fp32 + per-row max bits [8] u32.
-__host__ __device__ constexpr int xt_table_bytes(int K) { return (K / 64) * 1024 + 2 * (K / 64) * 32 + 64; }
+// Prepared x slices (vq_linear, 16-bit x, M <= 8): one slice per 512-wide
+// stage, [8 groups][8 rows][128 B] fp16 fragments, T [8 groups][8 rows] fp32
+// (f * group sums), -U [8 groups][4][4] fp32 (U = 1024 * the group sum of the
+// fp16 values, laid out as the MMA accumulator quad (row 2t, 2t+1, 2t, 2t+1)
+// of thread t), and 1/f [8 rows] fp32, with f a power of two per (stage,
+// row); the slice rides in the stage next to its weights.
+constexpr int kSliceT = 8 * 1024;
+constexpr int kSliceU = kSliceT + 8 * 8 * 4;
+constexpr int kSliceInv = kSliceU + 8 * 4 * 16;
+constexpr int kSliceBytes = kSliceInv + 8 * 4;
+__host__ __device__ constexpr int xs_stage_off_x() { return 2 * kWeightBoxBytes + 2 * kBN * 16; }
+__host__ __device__ constexpr int xs_stage_bytes() {
+  return (xs_stage_off_x() + kSliceBytes + 1023) / 1024 * 1024;
+}
+
+// x table [K/64 groups][8 rows][128 B] fp16, then T [K/64][8] fp32 and 1/f [8]
+// fp32 (this much is what a prepared table holds), then the build's scratch:
+// [K/64][8] fp32 and the row maxima [8] u32.
+__host__ __device__ constexpr int xt_prepared_bytes(int K) { return (K / 64) * 1024 + (K / 64) * 32 + 32; }
+__host__ __device__ constexpr int xt_table_bytes(int K) { return xt_prepared_bytes(K) + (K / 64) * 32 + 32; }
 constexpr int kMaxXtBytes = 96 * 1024;
 
 // Bytes of the per-block table of group sums X_g[m]: [K/64][8*MT] fp32.
@@ -123,9 +142,12 @@ struct GemmParams {
   int S;            // K splits per row block (1 = no split)
   int n_units;      // row blocks * S
   int D;            // pipeline depth (stages in the shared-memory ring)
+  int pre;          // stages whose weights are requested before griddepcontrol.wait
+  int red_alias;    // 1: the K-slice partials live in the stage ring (one unit per block)
   int stage_bytes;
   int off_x, off_s, off_b;   // offsets inside a stage (codes at 0)
-  int xt;           // 1: x-table variant (no x in the stages)
+  int xm;           // x source: 0 per-stage TMA, 1 per-block table, 2 prepared slices
+  const void* xprep;  // prepared slices [KT] (xm == 2), written by vq_prep_kernel
   int tab_bytes;    // bytes of the table region after the stage ring (1 KiB multiple)
   int x3d;          // 1: x arrives as one 3-D box per stage, 0: one box per group
                     // (same shared-memory layout either way: [group][8*MT rows][128 B],
@@ -720,7 +742,206 @@ __device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T
   });
 }
 
-template <int ACT, int MT, bool ARGMAX, bool XT>
+// The x slice of stage kt, row m, written by one warp: it reads the row's 512
+// values, picks the power-of-two scale f that brings their largest magnitude
+// into [2^13, 2^14) (no fp16 overflow whatever the activations' scale), and
+// writes the scaled fp16 fragments (odd nibble positions also divided by 16),
+// the f-scaled group sums T, -U and 1/f. Each slice is prepared once per call.
+template <int ACT>
+__device__ __forceinline__ void prep_slice_row(const void* __restrict__ x, int M, int K, int kt,
+                                               int m, int lane, uint8_t* __restrict__ slice) {
+  uint4 v[2];
+  float mx = 0.f, gs[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const int ci = lane + 32 * b;   // chunk of 8 values: group ci/8, position ci%8
+    v[b] = make_uint4(0u, 0u, 0u, 0u);
+    if (m < M)
+      v[b] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(x) +
+                                                  ((size_t)m * K + (size_t)kt * kBK + ci * 8) * 2));
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float xv = x_at<ACT>(v[b], i);
+      s += xv;
+      mx = fmaxf(mx, fabsf(xv));
+    }
+    gs[b] = s;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const float f = row_scale(__float_as_uint(mx));
+  float* T = reinterpret_cast<float*>(slice + kSliceT);
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const int ci = lane + 32 * b, j = ci >> 3, c = ci & 7;
+    uint32_t o4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float ph = (i & 1) ? 0.0625f : 1.f;
+      const __half2 hp =
+          __floats2half2_rn(x_at<ACT>(v[b], i) * f * ph, x_at<ACT>(v[b], i + 4) * f * ph);
+      o4[i] = *reinterpret_cast<const uint32_t*>(&hp);
+    }
+    *reinterpret_cast<uint4*>(slice + (j * 8 + m) * 128 + ((c ^ m) << 4)) =
+        make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    // the fp16 values exactly as the MMA will see them
+    float u = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&o4[i]));
+      u += h.x + h.y;
+    }
+    float s = gs[b];
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) {
+      s += __shfl_xor_sync(0xffffffffu, s, off);
+      u += __shfl_xor_sync(0xffffffffu, u, off);
+    }
+    if (c == 0) {
+      T[j * 8 + m] = f * s;
+      float* nu = reinterpret_cast<float*>(slice + kSliceU) + j * 16 + (m >> 1) * 4 + (m & 1);
+      nu[0] = -1024.f * u;
+      nu[2] = -1024.f * u;
+    }
+  }
+  if (lane == 0) reinterpret_cast<float*>(slice + kSliceInv)[m] = 1.f / f;
+}
+
+// The slices of one call: block kt prepares stage kt, one row per warp. It is
+// launched so that it may start while the kernel before it in the stream is
+// finishing, and waits for that kernel before it reads x or overwrites the
+// slices; the projection after it waits for it in the same way.
+constexpr int kPrepThreads = 256;   // 8 warps: the 8 rows of a stage
+
+template <int ACT>
+__global__ void __launch_bounds__(kPrepThreads)
+    vq_prep_kernel(const void* __restrict__ x, int M, int K, uint8_t* __restrict__ out) {
+  grid_launch_dependents();
+  grid_wait_prerequisites();
+  const int kt = blockIdx.x;
+  prep_slice_row<ACT>(x, M, K, kt, threadIdx.x >> 5, threadIdx.x & 31,
+                      out + (size_t)kt * kSliceBytes);
+}
+
+// Per-thread constants of the prepared-slice consumer (offsets in a stage).
+struct XsLane {
+  uint32_t w_even, w_odd;   // codes of the even / odd weight row of tile 0
+  uint32_t g3x32;           // (g % 4) * 32
+  uint32_t x_h0, x_h1;      // slice chunk of row g, first group of the K-slice, h = 0, 1
+  uint32_t sc;              // scales of the even row of tile 0 for the K-slice
+  uint32_t ts;              // T of (first group of the K-slice, row 2t)
+  uint32_t nu;              // -U quad of (first group of the K-slice, thread t)
+  uint32_t inv;             // 1/f of rows 2t, 2t+1
+};
+
+__device__ __forceinline__ XsLane xs_lane(int rw, int kq, int g, int t) {
+  using C = Cfg<1>;
+  XsLane o;
+  const int row = 16 * (C::RT * rw) + 2 * g;
+  const int box = (C::GPW == 4) ? kq * kWeightBoxBytes : 0;
+  o.w_even = box + row * 128 + ((t >> 1) << 4) + ((t & 1) << 3);
+  o.w_odd = box + (row + 1) * 128 + (((t >> 1) ^ 1) << 4) + ((t & 1) << 3);
+  o.g3x32 = (uint32_t)(g & 3) << 5;
+  const int j0 = kq * C::GPW;
+  o.x_h0 = xs_stage_off_x() + (j0 * 8 + g) * 128 + (((2 * t) ^ g) << 4);
+  o.x_h1 = xs_stage_off_x() + (j0 * 8 + g) * 128 + (((2 * t + 1) ^ g) << 4);
+  o.sc = xt_stage_off_s() + row * 16 + kq * C::GPW * 2;
+  o.ts = xs_stage_off_x() + kSliceT + (j0 * 8 + 2 * t) * 4;
+  o.nu = xs_stage_off_x() + kSliceU + (j0 * 4 + t) * 16;
+  o.inv = xs_stage_off_x() + kSliceInv + 2 * t * 4;
+  return o;
+}
+
+// One stage of the prepared-slice variant (MT = 1): the warp's K-slice of
+// groups for its RT row tiles, folded in the stage's scaled units and then
+// brought back with the slice's 1/f.
+template <int ACT>
+__device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
+                                                 float (&tot)[Cfg<1>::RT][1][4]) {
+  using C = Cfg<1>;
+  constexpr int RT = C::RT, GPW = C::GPW;
+  constexpr int kBiasOff = kBN * 16;
+  constexpr uint32_t kMagic16 = 0x64006400u;   // fp16 1024.0 in both halves
+  static_assert(GPW == 4 || GPW == 8, "K-slices of 4 or 8 groups");
+
+  Packed<GPW> sc0[RT], sc1[RT], bi0[RT], bi1[RT];
+  const uint32_t sa = sb + o.sc;
+  static_for<RT>([&](auto rc) {
+    constexpr int r = decltype(rc)::value;
+    sc0[r] = lds_packed_at<GPW, 256 * r>(sa);
+    sc1[r] = lds_packed_at<GPW, 256 * r + 16>(sa);
+    bi0[r] = lds_packed_at<GPW, 256 * r + kBiasOff>(sa);
+    bi1[r] = lds_packed_at<GPW, 256 * r + kBiasOff + 16>(sa);
+  });
+  const uint32_t we = sb + o.w_even, wo = sb + o.w_odd;
+  const uint32_t xa0 = sb + o.x_h0, xa1 = sb + o.x_h1;
+  const uint32_t ta = sb + o.ts;
+  float part[RT][4];
+#pragma unroll
+  for (int r = 0; r < RT; ++r) part[r][0] = part[r][1] = part[r][2] = part[r][3] = 0.f;
+
+  static_for<GPW>([&](auto jc) {
+    constexpr int jj = decltype(jc)::value;
+    constexpr int kBox = (GPW == 8 && jj >= 4) ? kWeightBoxBytes : 0;
+    const uint32_t sw = ((uint32_t)((jj & 3) << 5)) ^ o.g3x32;
+    const uint32_t ae = we + sw, ao = wo + sw;
+    uint2 wa[RT], wb[RT];
+    static_for<RT>([&](auto rc) {
+      constexpr int r = decltype(rc)::value;
+      wa[r] = lds64<kBox + 2048 * r>(ae);
+      wb[r] = lds64<kBox + 2048 * r>(ao);
+    });
+    const uint4 nuv = lds128<jj * 64>(sb + o.nu);
+    const float4 nu = make_float4(__uint_as_float(nuv.x), __uint_as_float(nuv.y),
+                                  __uint_as_float(nuv.z), __uint_as_float(nuv.w));
+    float acc[RT][4];
+    static_for<2>([&](auto hc) {
+      constexpr int h = decltype(hc)::value;
+      const uint4 bx = lds128<jj * 1024>(h ? xa1 : xa0);
+#pragma unroll
+      for (int r = 0; r < RT; ++r) {
+        const uint32_t qa = h ? wa[r].y : wa[r].x;
+        const uint32_t qb = h ? wb[r].y : wb[r].x;
+        const uint32_t qa8 = qa >> 8, qb8 = qb >> 8;
+        // codes as fp16 1024 + q (or 1024 + 16q): one AND/OR each; the
+        // accumulator starts at -U, which cancels the 1024s
+        const uint32_t a0[4] = {lop3_and_or(qa, 0x000F000Fu, kMagic16), lop3_and_or(qb, 0x000F000Fu, kMagic16),
+                                lop3_and_or(qa, 0x00F000F0u, kMagic16), lop3_and_or(qb, 0x00F000F0u, kMagic16)};
+        const uint32_t a1[4] = {lop3_and_or(qa8, 0x000F000Fu, kMagic16), lop3_and_or(qb8, 0x000F000Fu, kMagic16),
+                                lop3_and_or(qa8, 0x00F000F0u, kMagic16), lop3_and_or(qb8, 0x00F000F0u, kMagic16)};
+        float (&d)[4] = acc[r];
+        if (h == 0)
+          mma_16816_c<true>(d, a0, bx.x, bx.y, nu);
+        else
+          mma_16816<true>(d, a0, bx.x, bx.y);
+        mma_16816<true>(d, a1, bx.z, bx.w);
+      }
+    });
+    const uint2 tv = lds64<jj * 32>(ta);
+    const float T0 = __uint_as_float(tv.x), T1 = __uint_as_float(tv.y);
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+      const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
+      const float b_a = bf16_of(bi0[r], jj), b_b = bf16_of(bi1[r], jj);
+      part[r][0] = fmaf(s_a, acc[r][0], fmaf(b_a, T0, part[r][0]));
+      part[r][1] = fmaf(s_a, acc[r][1], fmaf(b_a, T1, part[r][1]));
+      part[r][2] = fmaf(s_b, acc[r][2], fmaf(b_b, T0, part[r][2]));
+      part[r][3] = fmaf(s_b, acc[r][3], fmaf(b_b, T1, part[r][3]));
+    }
+  });
+  const uint2 iv = lds64<0>(sb + o.inv);
+  const float i0 = __uint_as_float(iv.x), i1 = __uint_as_float(iv.y);
+#pragma unroll
+  for (int r = 0; r < RT; ++r) {
+    tot[r][0][0] = fmaf(i0, part[r][0], tot[r][0][0]);
+    tot[r][0][1] = fmaf(i1, part[r][1], tot[r][0][1]);
+    tot[r][0][2] = fmaf(i0, part[r][2], tot[r][0][2]);
+    tot[r][0][3] = fmaf(i1, part[r][3], tot[r][0][3]);
+  }
+}
+
+template <int ACT, int MT, bool ARGMAX, int XM>
 __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     vq_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_x,
@@ -728,6 +949,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   using C = Cfg<MT>;
   constexpr int MP = 8 * MT;
   constexpr int RT = C::RT, KQ = C::KQ, RW = C::RW, TEAMS = C::TEAMS, SLICES = C::SLICES;
+  constexpr bool XT = (XM == 1);   // x table built in the block
+  constexpr bool XS = (XM == 2);   // prepared x slices in the stages
   constexpr int kConsumers = C::WARPS;
   constexpr int kProducerWarp = kConsumers;
   constexpr int kXBoxes = (ACT == VQ_F32) ? 16 : 8;   // per-group boxes (x3d == 0)
@@ -746,19 +969,22 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 196);
   float* const red_v = reinterpret_cast<float*>(misc + 256);
   uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + 8 * 64 * 4);
-  float* const red_k = reinterpret_cast<float*>(misc + kMiscBytes);   // [SLICES-1][128][MP]
+  float* const red_k = p.red_alias ? reinterpret_cast<float*>(sbase)   // [SLICES-1][128][MP]
+                                   : reinterpret_cast<float*>(misc + misc_bytes(ARGMAX));
   float* const xsum = reinterpret_cast<float*>(tabs);   // [K/64][MP]
   const int KG = p.K / 64;
   XTab X;
   X.lines = smem_addr(tabs);
   X.T = reinterpret_cast<float*>(tabs + KG * 1024);
-  X.U = X.T + KG * 8;
-  X.inv_f = X.U + KG * 8;
-  X.rmax = reinterpret_cast<uint32_t*>(X.inv_f + 8);
+  X.inv_f = X.T + KG * 8;
+  X.U = X.inv_f + 8;
+  X.rmax = reinterpret_cast<uint32_t*>(X.U + KG * 8);
   auto full_bar = [&](int s) { return misc_a + 8u * s; };
   auto empty_bar = [&](int s) { return misc_a + 64u + 8u * s; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the next kernel in the stream may be scheduled as soon as SMs free up
+  grid_launch_dependents();
   const uint32_t x_bar = misc_a + 128u;   // x table landed (x-table variant)
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.D; ++s) {
@@ -781,6 +1007,51 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       prefetch_tensormap(&tm_s);
       prefetch_tensormap(&tm_b);
       prefetch_tensormap(&tm_x);
+      // Weights are constants of the model: the first stages' weights are
+      // requested before waiting for the kernel before this one in the stream
+      // (programmatic dependent launch), so the weight stream overlaps that
+      // kernel's tail. x, which that kernel may write, is requested only after
+      // the wait.
+      const uint64_t w_policy = l2_evict_first_policy();
+      auto issue_w = [&](int slot, int kt, int rb) {
+        const uint32_t sb = base + slot * p.stage_bytes;
+        const uint32_t fb = full_bar(slot);
+        mbar_arrive_expect_tx(fb, p.tx_bytes);
+        tma_load_2d_hint(sb, &tm_w, kt * (kBK / 8), rb * kBN, fb, w_policy);
+        tma_load_2d_hint(sb + kWeightBoxBytes, &tm_w, kt * (kBK / 8) + 32, rb * kBN, fb, w_policy);
+        tma_load_2d_hint(sb + p.off_s, &tm_s, kt * (kBK / 64), rb * kBN, fb, w_policy);
+        tma_load_2d_hint(sb + p.off_b, &tm_b, kt * (kBK / 64), rb * kBN, fb, w_policy);
+      };
+      auto issue_x = [&](int slot, int kt) {
+        const uint32_t sb = base + slot * p.stage_bytes;
+        const uint32_t fb = full_bar(slot);
+        if constexpr (XS) {
+          bulk_load(sb + p.off_x, static_cast<const uint8_t*>(p.xprep) + (size_t)kt * kSliceBytes,
+                    kSliceBytes, fb);
+        } else if constexpr (XT) {
+          // x comes from the block's table
+        } else if (p.x3d) {
+          tma_load_3d(sb + p.off_x, &tm_x, 0, 0, kt * kXBoxes, fb);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kXBoxes; ++j)
+            tma_load_2d(sb + p.off_x + j * MP * 128, &tm_x, kt * kBK + j * kXBoxElems, 0, fb);
+        }
+      };
+      int pre = 0;   // stages whose weights were issued before the wait
+      int kt_first = 0;
+      if (blockIdx.x < p.n_units) {
+        const int u0 = blockIdx.x;
+        const int rb = u0 / p.S, sp = u0 - rb * p.S;
+        const int kt0 = sp * p.KT / p.S, kt1 = (sp + 1) * p.KT / p.S;
+        kt_first = kt0;
+        for (int r = 0; r < p.pre && r < p.D && kt0 + r < kt1; ++r) {
+          issue_w(r, kt0 + r, rb);
+          ++pre;
+        }
+      }
+      grid_wait_prerequisites();
+      bool ok = true;
       if constexpr (XT) {
         // the block's x, all K/64 groups of 8 rows, first of all
         mbar_arrive_expect_tx(x_bar, (uint32_t)KG * 1024u);
@@ -791,33 +1062,24 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         }
       }
       int q = 0;
-      bool ok = true;
+      for (int r = 0; r < pre; ++r) issue_x(r, kt_first + r);
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         const int rb = u / p.S, sp = u - rb * p.S;
         const int kt0 = sp * p.KT / p.S, kt1 = (sp + 1) * p.KT / p.S;
         for (int kt = kt0; kt < kt1; ++kt) {
+          if (pre > 0) {   // weights issued before the wait, x just after it
+            --pre;
+            ++q;
+            continue;
+          }
           const int slot = q % p.D;
           const uint32_t ph = (uint32_t)(q / p.D) & 1u;
           if (!wait_or_abort(empty_bar(slot), ph ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          const uint32_t sb = base + slot * p.stage_bytes;
-          const uint32_t fb = full_bar(slot);
-          mbar_arrive_expect_tx(fb, p.tx_bytes);
-          tma_load_2d(sb, &tm_w, kt * (kBK / 8), rb * kBN, fb);
-          tma_load_2d(sb + kWeightBoxBytes, &tm_w, kt * (kBK / 8) + 32, rb * kBN, fb);
-          tma_load_2d(sb + p.off_s, &tm_s, kt * (kBK / 64), rb * kBN, fb);
-          tma_load_2d(sb + p.off_b, &tm_b, kt * (kBK / 64), rb * kBN, fb);
-          if constexpr (XT) {
-            // x comes from the block's table
-          } else if (p.x3d) {
-            tma_load_3d(sb + p.off_x, &tm_x, 0, 0, kt * kXBoxes, fb);
-          } else {
-#pragma unroll
-            for (int j = 0; j < kXBoxes; ++j)
-              tma_load_2d(sb + p.off_x + j * MP * 128, &tm_x, kt * kBK + j * kXBoxElems, 0, fb);
-          }
+          issue_w(slot, kt, rb);
+          issue_x(slot, kt);
           ++q;
         }
       }
@@ -848,12 +1110,17 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     }
 
   bool aborted = false;
+  // x and every output may belong to the kernel before this one in the stream
+  grid_wait_prerequisites();
   // group sums of x (or the whole x table) for all of K, while the first
   // stages are in flight
   LaneOffsets<ACT, MT> lo;
   XtLane xl;
   uint32_t xsum_a = 0, T_a = 0;
-  if constexpr (XT) {
+  XsLane xsl;
+  if constexpr (XS) {
+    xsl = xs_lane(rw, kq, g, t);
+  } else if constexpr (XT) {
     if (!wait_or_abort(x_bar, 0u, abort_flag, p.err)) aborted = true;
     build_xtab<ACT>(tabs, X, p, threadIdx.x, kConsumers * 32, kConsumers * 32);
     xl = xt_lane<MT>(X.lines, rw, kq, g, t);
@@ -887,7 +1154,9 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       const uint32_t ph = (uint32_t)phase;
       const bool ok = !aborted && wait_or_abort(full_bar(slot), ph, abort_flag, p.err);
       if (ok) {
-        if constexpr (XT)
+        if constexpr (XS)
+          consume_stage_xs<ACT>(base + slot * p.stage_bytes, xsl, tot);
+        else if constexpr (XT)
           consume_stage_xt<ACT>(base + slot * p.stage_bytes, kt, T_a, xl, tot);
         else
           consume_stage<ACT, MT>(base + slot * p.stage_bytes, xsum_a + kt * (8 * MP * 4), lo, tot);
@@ -904,6 +1173,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     }
 
     if constexpr (SLICES > 1) {
+      // partials in the stage ring: every team must be done with its stages
+      if (p.red_alias) named_bar_sync(1, kConsumers * 32);
       // slices 1.. publish their partial sums, slice 0 adds them in order
       if (slice > 0) {
 #pragma unroll
@@ -1090,14 +1361,39 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   }
 }
 
-template <int ACT, int MT, bool AM, bool XT = false>
+// Every kernel of the projection is launched with programmatic stream
+// serialization: it may be scheduled while the kernel before it in the stream
+// is finishing, and waits for that kernel (griddepcontrol.wait) before it
+// touches anything the kernel may have written.
+template <typename Kern, typename... Args>
+int launch_pdl(Kern k, dim3 grid, int threads, size_t smem, cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...) == cudaSuccess ? VQ_OK : VQ_ECUDA;
+}
+
+template <int ACT, int MT, bool AM, int XM = 0>
 int launch_one(const GemmLaunch& L) {
-  auto k = vq_gemm_kernel<ACT, MT, AM, XT>;
+  auto k = vq_gemm_kernel<ACT, MT, AM, XM>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem) !=
       cudaSuccess)
     return VQ_ECUDA;
-  k<<<L.grid, Cfg<MT>::THREADS, L.smem, L.stream>>>(L.tm_w, L.tm_s, L.tm_b, L.tm_x, L.p);
-  return cudaGetLastError() == cudaSuccess ? VQ_OK : VQ_ECUDA;
+  if constexpr (XM == 2 && ACT != VQ_F32) {
+    // the slices first; the projection may start before they are done
+    const int rc = launch_pdl(vq_prep_kernel<ACT>, dim3(L.p.KT), kPrepThreads, 0, L.stream,
+                              L.p.x, L.p.M, L.p.K, (uint8_t*)L.p.xprep);
+    if (rc != VQ_OK) return rc;
+  }
+  return launch_pdl(k, dim3(L.grid), Cfg<MT>::THREADS, L.smem, L.stream, L.tm_w, L.tm_s, L.tm_b,
+                    L.tm_x, L.p);
 }
 
 template <int ACT>
@@ -1114,9 +1410,13 @@ int launch_gemm_act(const GemmLaunch& L) {
         return VQ_EUNSUPPORTED;
     }
   } else {
-    if (L.p.xt) {
-      if (L.MT != 1) return VQ_EUNSUPPORTED;
-      return L.argmax ? launch_one<ACT, 1, true, true>(L) : launch_one<ACT, 1, false, true>(L);
+    if (L.p.xm == 1) {
+      if (L.MT != 1 || !L.argmax) return VQ_EUNSUPPORTED;
+      return launch_one<ACT, 1, true, 1>(L);
+    }
+    if (L.p.xm == 2) {
+      if (L.MT != 1 || L.argmax) return VQ_EUNSUPPORTED;
+      return launch_one<ACT, 1, false, 2>(L);
     }
     switch (L.MT) {
       VQ_CASE(1)
