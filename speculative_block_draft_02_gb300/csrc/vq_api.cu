@@ -3,6 +3,7 @@
 #include <mutex>
 
 #include "vq_gemm.cuh"
+#include "vq_tc.cuh"
 
 namespace vq {
 
@@ -152,6 +153,43 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   }
   p.n_units = p.RB * p.S;
   p.grid = p.n_units < sms ? p.n_units : sms;
+  //  xm = 3 (16-bit x, M > 16, no K split): the tensor-core (tcgen05)
+  //         kernel; x for the stage by TMA as for xm = 0, X_g from a small
+  //         kernel (vq_linear) or summed per block (arg max). Measured at
+  //         K=5120, N=17408: M=24..64 it beats the mma.sync kernel (27.6 vs
+  //         33.1 us at M=24, 33.8 vs 59.2 us at M=64); at M=16 it does not
+  //         (25.7 vs 20.6 us), its per-group MMA issue and handoffs cost more
+  //         than the 16-row mma.sync work they replace.
+  if (!f32 && p.MT >= 4 && p.S == 1) {
+    const int tab_tc = (int)round_up((size_t)tc_xs_bytes(K, p.MP), 1024);
+    const int sb = tc_stage_bytes(p.MP);
+    int D = (kSmemLimit - 1024 - kTcMiscBytes - tab_tc) / sb;
+    if (D > kMaxStages) D = kMaxStages;
+    if (D >= 2) {
+      p.xm = 3;
+      p.D = D;
+      p.pre = D < 3 ? D : 3;
+      p.stage_bytes = sb;
+      p.off_x = kTcOffX;
+      p.off_s = kTcOffS;
+      p.off_b = kTcOffB;
+      p.xbox_bytes = 128 * p.MP;
+      p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + 8 * 128 * p.MP);
+      p.tab_bytes = tab_tc;
+      p.red_alias = false;
+      p.smem = 1024 + (size_t)D * sb + tab_tc + kTcMiscBytes;
+      p.ws_cnt_bytes = 0;
+      if (argmax) {
+        p.ws_xp_bytes = 0;
+        p.ws_bytes = round_up((size_t)M * 8 + 4, 16);
+      } else {
+        p.ws_xp_bytes = round_up((size_t)tc_xs_bytes(K, p.MP), 256);
+        p.ws_bytes = p.ws_xp_bytes;
+      }
+      *pl = p;
+      return VQ_OK;
+    }
+  }
   // The K-slice partial sums are only needed after a unit's last stage: with
   // one unit per block they can share the stage ring instead of taking
   // shared memory of their own.

@@ -146,7 +146,8 @@ struct GemmParams {
   int red_alias;    // 1: the K-slice partials live in the stage ring (one unit per block)
   int stage_bytes;
   int off_x, off_s, off_b;   // offsets inside a stage (codes at 0)
-  int xm;           // x source: 0 per-stage TMA, 1 per-block table, 2 prepared slices
+  int xm;           // x source: 0 per-stage TMA, 1 per-block table, 2 prepared slices,
+                    // 3 per-stage TMA for the tensor-core (tcgen05) kernel
   const void* xprep;  // prepared slices [KT] (xm == 2), written by vq_prep_kernel
   int tab_bytes;    // bytes of the table region after the stage ring (1 KiB multiple)
   int x3d;          // 1: x arrives as one 3-D box per stage, 0: one box per group
@@ -1396,6 +1397,10 @@ int launch_one(const GemmLaunch& L) {
                     L.tm_x, L.p);
 }
 
+// The tensor-core (tcgen05) kernel for 16-bit x with M > 16 (vq_tc.cuh).
+template <int ACT, int MP, bool AM>
+int launch_tc(const GemmLaunch& L);
+
 template <int ACT>
 int launch_gemm_act(const GemmLaunch& L) {
 #define VQ_CASE(mt)                                                      \
@@ -1417,6 +1422,16 @@ int launch_gemm_act(const GemmLaunch& L) {
     if (L.p.xm == 2) {
       if (L.MT != 1 || L.argmax) return VQ_EUNSUPPORTED;
       return launch_one<ACT, 1, false, 2>(L);
+    }
+    if (L.p.xm == 3) {
+      switch (L.MT) {
+        case 4:
+          return L.argmax ? launch_tc<ACT, 32, true>(L) : launch_tc<ACT, 32, false>(L);
+        case 8:
+          return L.argmax ? launch_tc<ACT, 64, true>(L) : launch_tc<ACT, 64, false>(L);
+        default:
+          return VQ_EUNSUPPORTED;
+      }
     }
     switch (L.MT) {
       VQ_CASE(1)

@@ -96,6 +96,33 @@ def test_linear_wide_n_x_table(M, K, N, dtype):
     assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
 
 
+# 16-bit x with M > 16 and an N wide enough that K is not split: the
+# tensor-core (tcgen05) kernel, M padded to 32 / 64 rows
+TC_SHAPES = [(17, 512, 12345, "bf16"), (24, 1024, 10000, "f16"), (32, 1024, 9800, "f16"),
+             (33, 512, 9729, "bf16"), (40, 512, 9999, "bf16"), (64, 1024, 10001, "bf16"),
+             (64, 512, 9730, "f16")]
+
+
+@pytest.mark.parametrize("M,K,N,dtype", TC_SHAPES)
+def test_linear_tensor_core_path(M, K, N, dtype):
+    seed = 7 * M + K + N
+    w = synth.w4_weights(seed, N, K)
+    x = synth.activations(seed, M, K, dtype)
+    y = run_linear(x, w, dtype)
+    cols = _sample_cols(N, 5, 200)
+    assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
+
+
+@pytest.mark.parametrize("M,K,N,dtype", [(17, 512, 3000, "bf16"), (20, 1024, 9000, "f16"),
+                                         (64, 1024, 40000, "f16")])
+def test_vocab_argmax_tensor_core_path(M, K, N, dtype):
+    w = synth.w4_weights(M * 3 + N, N, K)
+    x = synth.activations(M * 3 + N, M, K, dtype)
+    idx, mx, ws = run_vocab(x, w, dtype)
+    check_argmax(idx, mx, oracle_linear(x, w, dtype))
+    assert not ws.any(), "workspace must be left zeroed"
+
+
 def test_linear_x_table_handles_large_and_tiny_rows():
     # the per-row fp16 scaling keeps rows of very different magnitude exact
     M, K, N = 4, 1024, 60000
