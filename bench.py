@@ -63,6 +63,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-path", action="store_true", help="skip the per-kernel path table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--rows", type=int, default=M, choices=[8, 64],
+                    help="rows of the timed verify projection: 8 (the headline block) or 64 "
+                         "(the next-block verify GEMM, B=4 x block 16)")
     return ap.parse_args()
 
 
@@ -225,9 +228,13 @@ def dev_act(seed, M_, K_, dtype="bf16", scale=1.0, name="x"):
 
 
 def launches_per_call(vq, M_, K_, N_):
-    # 16-bit x with M <= 8 and a workspace for the prepared x table: the table
-    # kernel, then the projection
-    return 2 if vq.vq_linear_workspace_bytes(M_, K_, N_, torch.bfloat16) >= 16 * K_ else 1
+    # 16-bit x: M <= 8 prepares the x slices, M > 16 (no K split) sums the x
+    # groups in a small kernel before the projection; with a K split there is
+    # no such kernel
+    if M_ <= 8:
+        return 2
+    nb = vq.vq_linear_workspace_bytes(M_, K_, N_, torch.bfloat16)
+    return 2 if M_ > 16 and nb == (K_ // 64) * 64 * 4 else 1
 
 
 def workspace_for(vq, M_, K_, N_, dt):
@@ -285,23 +292,25 @@ def run_ours(args):
     dev = torch.cuda.current_device()
     K_steps, W = args.steps, max(3, args.warmup)
 
-    # ---- headline: vq_linear M=8 K=5120 N=17408 bf16, rotating weight copies
-    b_main = alg_bytes(M, K, N)
+    # ---- headline: vq_linear M=8 (or --rows 64) K=5120 N=17408 bf16, rotating
+    # weight copies
+    Mr = args.rows
+    b_main = alg_bytes(Mr, K, N)
     n_cp = n_copies_for(b_main)
     w, copies = dev_weights(0, n_cp, N, K)
-    xb, x = dev_act(0, M, K)
-    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-    ws = workspace_for(vq, M, K, N, torch.bfloat16)
+    xb, x = dev_act(0, Mr, K)
+    y = torch.empty((Mr, N), dtype=torch.bfloat16, device="cuda")
+    ws = workspace_for(vq, Mr, K, N, torch.bfloat16)
     calls = [(lambda c=c: vq.vq_linear(x, *c, y=y, workspace=ws)) for c in copies]
 
     clocks = ClockSampler(dev)
     total, per_launch = time_calls(calls, K_steps, W, world)
     clk = clocks.stop()
 
-    rows_per_s = world * M * K_steps / total
+    rows_per_s = world * Mr * K_steps / total
     peak, peak_kind = measured_peaks()
     achieved = b_main / per_launch / 1e9
-    traffic = profiled_traffic("vq_linear_bf16_m8_k5120_n17408")
+    traffic = profiled_traffic("vq_linear_bf16_m%d_k5120_n17408" % Mr)
 
     # ---- e2e through the public binding, host buffers, copies every step
     x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -324,7 +333,7 @@ def run_ours(args):
         torch.cuda.current_stream().synchronize()
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
-    e2e = {"value": world * M * e2e_steps / t_e2e, "unit": "rows/s",
+    e2e = {"value": world * Mr * e2e_steps / t_e2e, "unit": "rows/s",
            "h2d_bytes_per_step": x.numel() * x.element_size(),
            "d2h_bytes_per_step": y.numel() * y.element_size(),
            "us_per_step": t_e2e / e2e_steps * 1e6}
@@ -334,7 +343,8 @@ def run_ours(args):
         "steps": K_steps, "warmup": W, "ms_per_step": total / K_steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": dict(CONFIG, parallelism="replicas" if world > 1 else "single",
+        "config": dict(CONFIG, workload="verify_w4_m%d_k5120_n17408" % Mr, M=Mr,
+                       parallelism="replicas" if world > 1 else "single",
                        l2="inputs > L2: %d rotating weight copies (%.0f MB)"
                           % (n_cp, n_cp * b_main / 1e6),
                        timing="CUDA graphs of %d launches, events on the launch stream"
@@ -342,9 +352,14 @@ def run_ours(args):
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes": b_main, "kernel": "vq_gemm_kernel<bf16,MT=1>",
-                     "us_per_launch": per_launch * 1e6},
-        "e2e": e2e, "gpu_launches": K_steps * launches_per_call(vq, M, K, N), "clocks": clk,
+                     "algorithmic_bytes": b_main,
+                     "kernel": ("vq_gemm_kernel<bf16, MT=1, prepared x slices>" if Mr <= 8 else
+                                "vq_tc_kernel<bf16, MP=64> (tcgen05)"),
+                     "us_per_launch": per_launch * 1e6,
+                     "launch_note": "per call: a small x-preparation kernel, then the "
+                                    "projection, chained by programmatic dependent launch; "
+                                    "time per call over the timed region"},
+        "e2e": e2e, "gpu_launches": K_steps * launches_per_call(vq, Mr, K, N), "clocks": clk,
     }
 
     if not args.no_path:
@@ -453,10 +468,11 @@ def cpu_baseline_full(w, xb, budget_s=12.0):
     for _ in range(reps):
         oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16)
     t = time.perf_counter() - t0
-    return {"value": M * reps / t, "unit": "rows/s", "cores": oracle.num_threads(),
+    rows = xb.shape[0]
+    return {"value": rows * reps / t, "unit": "rows/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": "full M=8 K=5120 N=17408 bf16 step, %d repeats, fp64 scalar C, OpenMP over"
-                      " output columns" % reps}
+            "sample": "full M=%d K=5120 N=17408 bf16 step, %d repeats, fp64 scalar C, OpenMP "
+                      "over output columns" % (rows, reps)}
 
 
 # ----------------------------------------------------------------------------- reference arm
