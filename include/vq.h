@@ -126,6 +126,29 @@ int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_t* qw,
                     void* stream);
 
 /*
+ * Vocabulary projection with the fused arg max and the runner-up logit.
+ *
+ * Source: ds4 #778 "dspark: fold first-token forward into verify ...", PR
+ * description (the margin gate: the drafter does not propose where the
+ * target's top-1/top-2 logit margin shows that the target is hesitating).
+ *
+ * The same operation, arguments and results as vq_vocab_argmax, plus
+ *   second[m] = the largest logits[m][n] over n != argmax[m] in fp32 (NaN
+ *               logits skipped; -inf when the row has no other non-NaN
+ *               logit); an exact tie for the maximum gives second = maxval.
+ * so that maxval[m] - second[m] is the top-1/top-2 margin.
+ * second     float [M] on the device, required.
+ * workspace  vq_vocab_argmax_top2_workspace_bytes(M) bytes (528 + 4096*M at
+ *            most), 16-byte aligned, zero-filled before its first use; the
+ *            part that must start at zero is left zero-filled by every call.
+ */
+size_t vq_vocab_argmax_top2_workspace_bytes(int M);
+int vq_vocab_argmax_top2(const void* x, int M, int K, int N, const uint32_t* qw,
+                         const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                         int32_t* argmax, float* maxval, float* second, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * vq_vocab_argmax without a workspace: the same operation, arguments and
  * results as vq_vocab_argmax, but its scratch memory (M*8 + 4 bytes, rounded
  * up to 16) lives in a fixed 1 KiB array inside this library, so the call

@@ -28,6 +28,8 @@ SIGNATURES = {
     "vq_vocab_argmax_workspace_bytes": (_S, [_I]),
     "vq_vocab_argmax": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _S, _P]),
     "vq_vocab_argmax_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
+    "vq_vocab_argmax_top2_workspace_bytes": (_S, [_I]),
+    "vq_vocab_argmax_top2": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P]),
     "verify_accept_walk": (_I, [_P, _P, _I, _I, _P, _P]),
     "kv_compact_per_row": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
     "vq_strerror": (ctypes.c_char_p, [_I]),
@@ -111,6 +113,30 @@ def vq_vocab_argmax(x, qw, scales, biases, workspace, argmax=None, maxval=None, 
                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "vq_vocab_argmax")
     return argmax, maxval
+
+
+def vq_vocab_argmax_top2_workspace_bytes(M: int) -> int:
+    return int(lib().vq_vocab_argmax_top2_workspace_bytes(M))
+
+
+def vq_vocab_argmax_top2(x, qw, scales, biases, workspace, argmax=None, maxval=None, second=None,
+                         stream=None):
+    """(argmax int32[M], maxval float32[M], second float32[M]): the arg max and the
+    runner-up logit of x @ dequant(W)^T, logits never stored."""
+    M, K = x.shape
+    N = qw.shape[0]
+    if argmax is None:
+        argmax = torch.empty(M, dtype=torch.int32, device=x.device)
+    if maxval is None:
+        maxval = torch.empty(M, dtype=torch.float32, device=x.device)
+    if second is None:
+        second = torch.empty(M, dtype=torch.float32, device=x.device)
+    rc = lib().vq_vocab_argmax_top2(_ptr(x), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
+                                    _ACT[x.dtype], _ptr(argmax), _ptr(maxval), _ptr(second),
+                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream))
+    _check(rc, "vq_vocab_argmax_top2")
+    return argmax, maxval, second
 
 
 def vq_vocab_argmax_noalloc(x, qw, scales, biases, argmax=None, maxval=None, stream=None):

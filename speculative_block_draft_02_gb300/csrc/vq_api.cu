@@ -259,23 +259,33 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   return VQ_OK;
 }
 
+// Blocks whose top-2 candidates the workspace of vq_vocab_argmax_top2 holds;
+// the arg max grid is capped to it (it is persistent over row blocks).
+constexpr int kMaxTop2Blocks = 256;
+
 int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint16_t* scales,
              const uint16_t* biases, int act, bool argmax, void* y, int32_t* amax, float* maxval,
-             void* ws, size_t ws_bytes, void* stream) {
+             void* ws, size_t ws_bytes, void* stream, float* second = nullptr) {
   int rc = check_shape(M, K, N, act);
   if (rc) return rc;
   if (!x || !qw || !scales || !biases) return VQ_EINVAL;
   if (argmax ? !amax : !y) return VQ_EINVAL;
   if (((uintptr_t)x | (uintptr_t)qw | (uintptr_t)scales | (uintptr_t)biases) & 15u)
     return VQ_EALIGN;
-  if (((uintptr_t)y | (uintptr_t)amax | (uintptr_t)maxval) & 3u) return VQ_EALIGN;
+  if (((uintptr_t)y | (uintptr_t)amax | (uintptr_t)maxval | (uintptr_t)second) & 3u)
+    return VQ_EALIGN;
   int sms;
   int32_t* err;
   if ((rc = device_state(&sms, &err))) return rc;
   Plan pl;
   if ((rc = make_plan(M, K, N, act, argmax, sms, &pl))) return rc;
-  if (pl.ws_bytes) {
-    if (!ws || ws_bytes < pl.ws_bytes) return VQ_EWORKSPACE;
+  size_t need = pl.ws_bytes;
+  if (second) {
+    if (pl.grid > kMaxTop2Blocks) pl.grid = kMaxTop2Blocks;
+    need = round_up((size_t)M * 8 + 4, 16) + (size_t)kMaxTop2Blocks * M * 16;
+  }
+  if (need) {
+    if (!ws || ws_bytes < need) return VQ_EWORKSPACE;
     if ((uintptr_t)ws & 15u) return VQ_EALIGN;
   }
 
@@ -307,6 +317,10 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
     p.done = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + (size_t)M * 8);
     p.argmax = amax;
     p.maxval = maxval;
+    if (second) {
+      p.second = second;
+      p.cand = reinterpret_cast<uint4*>(static_cast<char*>(ws) + round_up((size_t)M * 8 + 4, 16));
+    }
   } else {
     if (pl.ws_xp_bytes) p.xprep = ws;
     if (pl.S > 1) {
@@ -393,6 +407,20 @@ extern "C" int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_
                                size_t workspace_bytes, void* stream) {
   return run_gemm(x, M, K, N, qw, scales, biases, act_dtype, true, nullptr, argmax, maxval,
                   workspace, workspace_bytes, stream);
+}
+
+extern "C" size_t vq_vocab_argmax_top2_workspace_bytes(int M) {
+  if (M < 1 || M > 64) return 0;
+  return round_up((size_t)M * 8 + 4, 16) + (size_t)kMaxTop2Blocks * M * 16;
+}
+
+extern "C" int vq_vocab_argmax_top2(const void* x, int M, int K, int N, const uint32_t* qw,
+                                    const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                                    int32_t* argmax, float* maxval, float* second,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!second) return VQ_EINVAL;
+  return run_gemm(x, M, K, N, qw, scales, biases, act_dtype, true, nullptr, argmax, maxval,
+                  workspace, workspace_bytes, stream, second);
 }
 
 // ---------------------------------------------------------------- no-alloc arg max

@@ -66,7 +66,7 @@ constexpr int kMaxStages = 8;
 constexpr int kWeightBoxBytes = kBN * 128;   // 128 rows x 32 words
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per block
 // misc area after the stage ring: 2 x 8 mbarriers, flags, arg max scratch
-constexpr int kMiscBytes = 256 + 2 * 8 * 64 * 4;
+constexpr int kMiscBytes = 256 + 3 * 8 * 64 * 4;
 // bytes of the misc region: the arg max's cross-warp buffers only with ARGMAX
 __host__ __device__ constexpr int misc_bytes(bool argmax) { return argmax ? kMiscBytes : 256; }
 
@@ -161,6 +161,8 @@ struct GemmParams {
   uint32_t* done;              // arg max block counter
   int32_t* argmax;
   float* maxval;
+  float* second;               // runner-up logit [M] (top-2 arg max), or null
+  uint4* cand;                 // per-block (best, index, runner-up) [grid][M], or null
   int32_t* err;
 };
 
@@ -298,6 +300,47 @@ __device__ __forceinline__ bool better(float v, uint32_t n, bool has, float bv, 
   if (!has) return false;
   if (!bhas) return true;
   return v > bv || (v == bv && n < bn);
+}
+
+// Merges candidate (ov, on, oh, os) into (v, n, h, s): the best by value, ties
+// to the lower index, and as runner-up the largest of the other values
+// (-inf when there is none). A candidate without a value (oh false) only
+// contributes its runner-up, which is then -inf too.
+__device__ __forceinline__ void top2_merge(float& v, uint32_t& n, bool& h, float& s, float ov,
+                                           uint32_t on, bool oh, float os) {
+  if (better(ov, on, oh, v, n, h)) {
+    s = fmaxf(os, h ? v : -INFINITY);
+    v = ov;
+    n = on;
+    h = true;
+  } else {
+    s = fmaxf(s, fmaxf(os, oh ? ov : -INFINITY));
+  }
+}
+
+// The last block's decode of row m: arg max and maximum from the packed key,
+// and (top-2 calls) the runner-up from every block's candidate: the block
+// that holds the winning index gives its own runner-up, every other block
+// its best.
+__device__ __forceinline__ void argmax_decode(const GemmParams& p, int m, unsigned long long key,
+                                              int nblocks) {
+  const uint32_t n1 = key == 0ull ? 0xFFFFFFFFu : 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+  if (key == 0ull) {
+    p.argmax[m] = 0;
+    if (p.maxval) p.maxval[m] = __uint_as_float(0x7FC00000u);
+  } else {
+    p.argmax[m] = (int32_t)n1;
+    if (p.maxval) p.maxval[m] = float_from_order((uint32_t)(key >> 32));
+  }
+  if (p.second) {
+    float sec = -INFINITY;
+    for (int c = 0; c < nblocks; ++c) {
+      const uint4 e = __ldcg(p.cand + (size_t)c * p.M + m);
+      if (e.y == 0xFFFFFFFFu) continue;   // no value of row m in that block
+      sec = fmaxf(sec, e.y == n1 ? __uint_as_float(e.z) : __uint_as_float(e.x));
+    }
+    p.second[m] = sec;
+  }
 }
 
 // Per-thread constants of a consumer: 32-bit shared-memory offsets that do
@@ -970,6 +1013,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 196);
   float* const red_v = reinterpret_cast<float*>(misc + 256);
   uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + 8 * 64 * 4);
+  float* const red_s = reinterpret_cast<float*>(misc + 256 + 2 * 8 * 64 * 4);
   float* const red_k = p.red_alias ? reinterpret_cast<float*>(sbase)   // [SLICES-1][128][MP]
                                    : reinterpret_cast<float*>(misc + misc_bytes(ARGMAX));
   float* const xsum = reinterpret_cast<float*>(tabs);   // [K/64][MP]
@@ -1101,6 +1145,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   float best_v[MT][2];
   uint32_t best_n[MT][2];
   bool best_has[MT][2];
+  float best_s[MT][2];   // runner-up value (-inf: none yet)
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -1108,6 +1153,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       best_v[mt][c] = 0.f;
       best_n[mt][c] = 0u;
       best_has[mt][c] = false;
+      best_s[mt][c] = -INFINITY;
     }
 
   bool aborted = false;
@@ -1283,9 +1329,12 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
             const float v = tot[r][mt][e] + 0.0f;   // -0 -> +0
             if (!aborted && n < p.N && !(v != v)) {
               if (!best_has[mt][c] || v > best_v[mt][c]) {
+                if (best_has[mt][c]) best_s[mt][c] = fmaxf(best_s[mt][c], best_v[mt][c]);
                 best_v[mt][c] = v;
                 best_n[mt][c] = (uint32_t)n;
                 best_has[mt][c] = true;
+              } else {
+                best_s[mt][c] = fmaxf(best_s[mt][c], v);
               }
             }
           }
@@ -1302,43 +1351,41 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
         float v = best_v[mt][c];
         uint32_t n = best_n[mt][c];
         bool h = best_has[mt][c];
+        float sv = best_s[mt][c];
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
           const float ov = __shfl_xor_sync(0xffffffffu, v, off);
           const uint32_t on = __shfl_xor_sync(0xffffffffu, n, off);
           const bool oh = __shfl_xor_sync(0xffffffffu, (int)h, off) != 0;
-          if (better(ov, on, oh, v, n, h)) {
-            v = ov;
-            n = on;
-            h = true;
-          }
+          const float os = __shfl_xor_sync(0xffffffffu, sv, off);
+          top2_merge(v, n, h, sv, ov, on, oh, os);
         }
         if (g == 0) {
           const int m = 8 * mt + 2 * t + c;
           red_v[rw * 64 + m] = v;
           red_i[rw * 64 + m] = h ? n : 0xFFFFFFFFu;
+          red_s[rw * 64 + m] = sv;
         }
       }
     named_bar_sync(2, kEpiThreads);
     if (threadIdx.x < MP) {
       const int m = threadIdx.x;
-      float v = 0.f;
+      float v = 0.f, sv = -INFINITY;
       uint32_t n = 0u;
       bool h = false;
       for (int w = 0; w < RW; ++w) {
         const uint32_t on = red_i[w * 64 + m];
-        const float ov = red_v[w * 64 + m];
-        if (better(ov, on, on != 0xFFFFFFFFu, v, n, h)) {
-          v = ov;
-          n = on;
-          h = true;
-        }
+        top2_merge(v, n, h, sv, red_v[w * 64 + m], on, on != 0xFFFFFFFFu, red_s[w * 64 + m]);
       }
       if (h && m < p.M && !aborted) {
         const unsigned long long key =
             ((unsigned long long)float_order(v) << 32) | (unsigned long long)(0xFFFFFFFFu - n);
         atomicMax(p.keys + m, key);
       }
+      if (p.cand && m < p.M)
+        p.cand[(size_t)blockIdx.x * p.M + m] =
+            make_uint4(__float_as_uint(v), (h && !aborted) ? n : 0xFFFFFFFFu,
+                       __float_as_uint(sv), 0u);
     }
     __threadfence();
     named_bar_sync(2, kEpiThreads);
@@ -1346,17 +1393,8 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     named_bar_sync(2, kEpiThreads);
     if (*epi_flag) {
       __threadfence();
-      if (threadIdx.x < p.M) {
-        const int m = threadIdx.x;
-        const unsigned long long key = atomicExch(p.keys + m, 0ull);
-        if (key == 0ull) {
-          p.argmax[m] = 0;
-          if (p.maxval) p.maxval[m] = __uint_as_float(0x7FC00000u);
-        } else {
-          p.argmax[m] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-          if (p.maxval) p.maxval[m] = float_from_order((uint32_t)(key >> 32));
-        }
-      }
+      if (threadIdx.x < p.M)
+        argmax_decode(p, threadIdx.x, atomicExch(p.keys + threadIdx.x, 0ull), gridDim.x);
       if (threadIdx.x == 0) *p.done = 0u;
     }
   }

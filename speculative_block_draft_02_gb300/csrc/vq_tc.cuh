@@ -230,8 +230,47 @@ constexpr int kTcOffB = kTcOffS + kBN * 16;
 constexpr int kTcOffX = kTcOffB + kBN * 16;   // 36864: 1 KiB aligned
 __host__ __device__ constexpr int tc_stage_bytes(int MP) { return kTcOffX + 8 * MP * 128; }
 __host__ __device__ constexpr int tc_xs_bytes(int K, int MP) { return (K / 64) * MP * 4; }
-// misc: mbarriers and flags (256 B), arg max scratch [4][64] value + index
-constexpr int kTcMiscBytes = 256 + 2 * 4 * 64 * 4;
+// misc: mbarriers and flags (256 B), arg max scratch [4][64] value, index, runner-up
+constexpr int kTcMiscBytes = 256 + 3 * 4 * 64 * 4;
+
+// Best row, its value and the runner-up value over the warp's 32 rows for each
+// of its HC columns, by halving: at offset o (16, 8, ...) a lane keeps the
+// half of its current columns selected by its lane bit o and merges in the
+// partner's values for them; once one column is left, the remaining offsets
+// merge whole. Lane l ends with column l / (32 / HC). Index 0xFFFFFFFF = no value.
+template <int HC>
+__device__ __forceinline__ void warp_top2_columns(float (&v)[HC], uint32_t (&n)[HC],
+                                                  float (&s)[HC], int lane) {
+  int o = 16;
+#pragma unroll
+  for (int cur = HC; cur > 1; cur >>= 1, o >>= 1) {
+    const bool hi = (lane & o) != 0;
+    const int half = cur >> 1;
+#pragma unroll
+    for (int j = 0; j < half; ++j) {
+      const float rv = __shfl_xor_sync(0xffffffffu, hi ? v[j] : v[j + half], o);
+      const uint32_t rn = __shfl_xor_sync(0xffffffffu, hi ? n[j] : n[j + half], o);
+      const float rs = __shfl_xor_sync(0xffffffffu, hi ? s[j] : s[j + half], o);
+      float kv = hi ? v[j + half] : v[j];
+      uint32_t kn = hi ? n[j + half] : n[j];
+      float ks = hi ? s[j + half] : s[j];
+      bool kh = kn != 0xFFFFFFFFu;
+      top2_merge(kv, kn, kh, ks, rv, rn, rn != 0xFFFFFFFFu, rs);
+      v[j] = kv;
+      n[j] = kh ? kn : 0xFFFFFFFFu;
+      s[j] = ks;
+    }
+  }
+#pragma unroll
+  for (; o >= 1; o >>= 1) {
+    const float rv = __shfl_xor_sync(0xffffffffu, v[0], o);
+    const uint32_t rn = __shfl_xor_sync(0xffffffffu, n[0], o);
+    const float rs = __shfl_xor_sync(0xffffffffu, s[0], o);
+    bool kh = n[0] != 0xFFFFFFFFu;
+    top2_merge(v[0], n[0], kh, s[0], rv, rn, rn != 0xFFFFFFFFu, rs);
+    if (!kh) n[0] = 0xFFFFFFFFu;
+  }
+}
 
 template <int ACT, int MP, bool ARGMAX>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -268,6 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 244);
   float* const red_v = reinterpret_cast<float*>(misc + 256);
   uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + 4 * 64 * 4);
+  float* const red_s = reinterpret_cast<float*>(misc + 256 + 2 * 4 * 64 * 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the next kernel in the stream may be scheduled as soon as SMs free up
@@ -489,7 +529,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else {
       if (!wait_or_abort(xs_bar, 0u, abort_flag, p.err)) aborted = true;
     }
-    float run_v = 0.f;
+    float run_v = 0.f, run_s = -INFINITY;
     uint32_t run_n = 0u;
     bool run_h = false;
     int q = 0;
@@ -568,57 +608,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       } else {
-        // best row n of this warp for each of its columns m; lane i keeps
-        // the running best of column HC*ch + i (n grows, so ties keep the
-        // lowest n)
+        // best row of this unit, its value and the runner-up for each of the
+        // warp's columns; lane l keeps the running ones of column
+        // HC*ch + l / (32 / HC) (rows grow with the unit, so ties keep the
+        // lowest row)
+        uint32_t cn[HC];
+        float cs[HC];
 #pragma unroll
         for (int i = 0; i < HC; ++i) {
-          float v = tot[i] + 0.0f;   // -0 -> +0
-          uint32_t vn = (uint32_t)n;
-          bool vh = !aborted && n < p.N && !(v != v);
-#pragma unroll
-          for (int off = 1; off < 32; off <<= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, v, off);
-            const uint32_t on = __shfl_xor_sync(0xffffffffu, vn, off);
-            const bool oh = __shfl_xor_sync(0xffffffffu, (int)vh, off) != 0;
-            if (better(ov, on, oh, v, vn, vh)) {
-              v = ov;
-              vn = on;
-              vh = true;
-            }
-          }
-          if (lane == i && better(v, vn, vh, run_v, run_n, run_h)) {
-            run_v = v;
-            run_n = vn;
-            run_h = true;
-          }
+          tot[i] += 0.0f;   // -0 -> +0
+          cn[i] = (!aborted && n < p.N && !(tot[i] != tot[i])) ? (uint32_t)n : 0xFFFFFFFFu;
+          cs[i] = -INFINITY;
         }
+        warp_top2_columns<HC>(tot, cn, cs, lane);
+        top2_merge(run_v, run_n, run_h, run_s, tot[0], cn[0], cn[0] != 0xFFFFFFFFu, cs[0]);
       }
     }
     if constexpr (ARGMAX) {
-      if (lane < HC) {
-        red_v[qd * 64 + HC * ch + lane] = run_v;
-        red_i[qd * 64 + HC * ch + lane] = run_h ? run_n : 0xFFFFFFFFu;
+      if (lane % (32 / HC) == 0) {
+        const int col = HC * ch + lane / (32 / HC);
+        red_v[qd * 64 + col] = run_v;
+        red_i[qd * 64 + col] = run_h ? run_n : 0xFFFFFFFFu;
+        red_s[qd * 64 + col] = run_s;
       }
       named_bar_sync(1, kTcFoldWarps * 32);
       if (ft < MP) {
-        float v = 0.f;
+        float v = 0.f, vs = -INFINITY;
         uint32_t vn = 0u;
         bool vh = false;
         for (int w = 0; w < 4; ++w) {
           const uint32_t on = red_i[w * 64 + ft];
-          const float ov = red_v[w * 64 + ft];
-          if (better(ov, on, on != 0xFFFFFFFFu, v, vn, vh)) {
-            v = ov;
-            vn = on;
-            vh = true;
-          }
+          top2_merge(v, vn, vh, vs, red_v[w * 64 + ft], on, on != 0xFFFFFFFFu, red_s[w * 64 + ft]);
         }
         if (vh && ft < p.M && !aborted) {
           const unsigned long long key =
               ((unsigned long long)float_order(v) << 32) | (unsigned long long)(0xFFFFFFFFu - vn);
           atomicMax(p.keys + ft, key);
         }
+        if (p.cand && ft < p.M)
+          p.cand[(size_t)blockIdx.x * p.M + ft] =
+              make_uint4(__float_as_uint(v), (vh && !aborted) ? vn : 0xFFFFFFFFu,
+                         __float_as_uint(vs), 0u);
       }
       __threadfence();
       named_bar_sync(1, kTcFoldWarps * 32);
@@ -626,16 +656,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       named_bar_sync(1, kTcFoldWarps * 32);
       if (*epi_flag) {
         __threadfence();
-        if (ft < p.M) {
-          const unsigned long long key = atomicExch(p.keys + ft, 0ull);
-          if (key == 0ull) {
-            p.argmax[ft] = 0;
-            if (p.maxval) p.maxval[ft] = __uint_as_float(0x7FC00000u);
-          } else {
-            p.argmax[ft] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
-            if (p.maxval) p.maxval[ft] = float_from_order((uint32_t)(key >> 32));
-          }
-        }
+        if (ft < p.M) argmax_decode(p, ft, atomicExch(p.keys + ft, 0ull), gridDim.x);
         if (ft == 0) *p.done = 0u;
       }
     }

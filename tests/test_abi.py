@@ -60,6 +60,11 @@ def test_vocab_workspace_size(vqlib):
     assert vqlib.vq_vocab_argmax_workspace_bytes(1) == 16
     assert vqlib.vq_vocab_argmax_workspace_bytes(0) == 0
     assert vqlib.vq_vocab_argmax_workspace_bytes(65) == 0
+    # keys and counter, then one 16-byte candidate per (block, row), 256 blocks
+    assert vqlib.vq_vocab_argmax_top2_workspace_bytes(64) == 528 + 256 * 64 * 16
+    assert vqlib.vq_vocab_argmax_top2_workspace_bytes(1) == 16 + 256 * 16
+    assert vqlib.vq_vocab_argmax_top2_workspace_bytes(0) == 0
+    assert vqlib.vq_vocab_argmax_top2_workspace_bytes(65) == 0
 
 
 def test_host_validation_rejects_before_any_launch(vqlib):
@@ -77,6 +82,11 @@ def test_host_validation_rejects_before_any_launch(vqlib):
     assert vqlib.vq_linear(P(0x1002), 8, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -2
     assert vqlib.vq_vocab_argmax(fake, 8, 512, 16, fake, fake, fake, 0, None, None, fake, 64,
                                  None) == -1
+    # the top-2 call needs its runner-up output, 4-byte aligned
+    assert vqlib.vq_vocab_argmax_top2(fake, 8, 512, 16, fake, fake, fake, 0, fake, None, None,
+                                      fake, 1 << 20, None) == -1
+    assert vqlib.vq_vocab_argmax_top2(fake, 8, 512, 16, fake, fake, fake, 0, fake, None,
+                                      P(0x1001), fake, 1 << 20, None) == -2
     assert vqlib.verify_accept_walk(fake, fake, 0, 8, fake, None) == -1
     assert vqlib.verify_accept_walk(fake, fake, 4, 0, fake, None) == -1
     assert vqlib.verify_accept_walk(P(0x1001), fake, 4, 8, fake, None) == -2

@@ -270,6 +270,66 @@ def test_vocab_argmax_ragged(M, K, N):
     check_argmax(idx, mx, oracle_linear(x, w, "bf16"))
 
 
+def run_vocab_top2(x_bits, w, dtype="bf16"):
+    x = to_dev_act(x_bits, dtype)
+    qw, s, b = to_dev_weights(w)
+    M = x.shape[0]
+    ws = torch.zeros(vq.vq_vocab_argmax_top2_workspace_bytes(M), dtype=torch.uint8,
+                     device="cuda")
+    idx, mx, sec = vq.vq_vocab_argmax_top2(x, qw, s, b, ws)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), mx.cpu().numpy(), sec.cpu().numpy(), ws, M
+
+
+def check_runner_up(idx, sec, logits):
+    """The runner-up must be the largest fp32 logit at any index other than
+    the one the kernel picked, within the fp32 accumulation error."""
+    f = logits.astype(np.float32)
+    for m in range(len(idx)):
+        row = np.delete(f[m], idx[m])
+        row = row[~np.isnan(row)]
+        want = row.max() if row.size else -np.inf
+        if np.isinf(want):
+            assert sec[m] == want
+        else:
+            assert abs(float(sec[m]) - float(want)) <= 1e-5 * max(1.0, abs(float(want))), (m, sec[m], want)
+
+
+# every arg max kernel: x table (M <= 8, wide N), per-stage x (M <= 16, fp32 x),
+# tcgen05 (16-bit x, M > 16)
+@pytest.mark.parametrize("M,K,N,dtype", [(8, 512, 60000, "bf16"), (3, 1024, 5000, "f16"),
+                                         (12, 512, 3001, "bf16"), (7, 512, 2000, "f32"),
+                                         (24, 1024, 9000, "bf16"), (64, 512, 20000, "f16")])
+def test_vocab_argmax_top2(M, K, N, dtype):
+    w = synth.w4_weights(M * 5 + N, N, K)
+    x = synth.activations(M * 5 + N, M, K, dtype)
+    idx, mx, sec, ws, _ = run_vocab_top2(x, w, dtype)
+    logits = oracle_linear(x, w, dtype)
+    check_argmax(idx, mx, logits)
+    check_runner_up(idx, sec, logits)
+    assert np.all(sec <= mx)
+    assert not ws[: vq.vq_vocab_argmax_workspace_bytes(M)].any(), "keys must be left zeroed"
+    # the same arg max as the call without the runner-up
+    idx2, mx2, _ = run_vocab(x, w, dtype)
+    assert np.array_equal(idx, idx2) and np.array_equal(mx, mx2)
+
+
+def test_vocab_argmax_top2_exact_tie_and_single_column():
+    N, K, M = 3000, 512, 20
+    w = synth.w4_weights(37, N, K)
+    x = synth.activations(37, M, K, "bf16")
+    r_idx, _, _ = oracle.argmax(oracle_linear(x, w, "bf16"))
+    a = int(r_idx[0])
+    lo = 5 if a > 5 else N - 1
+    for arr in (w.qw, w.scales, w.biases):
+        arr[lo] = arr[a]
+    idx, mx, sec, _, _ = run_vocab_top2(x, w)
+    assert idx[0] == min(lo, a) and sec[0] == mx[0], "a tie for the maximum: margin 0"
+    w1 = synth.w4_weights(38, 1, K)
+    idx, mx, sec, _, _ = run_vocab_top2(synth.activations(38, 4, K, "bf16"), w1)
+    assert np.all(idx == 0) and np.all(sec == -np.inf)
+
+
 def test_vocab_argmax_full_workload_and_accept():
     # M=64 (B=4 x block 16), K=2560, N=151936 vocab; drafts match the target
     # with p=0.7 per position until the first miss

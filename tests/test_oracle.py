@@ -238,7 +238,28 @@ def test_argmax_hand_cases(oracle_mod):
     idx, mx, sec = oracle_mod.argmax(np.array(rows))
     assert idx.tolist() == [0, 1, 3, 2, 0, 1, 0, 0, 2]
     assert mx[1] == 5.0 and mx[3] == -3.0 and np.isnan(mx[6])
-    assert sec[1] == 5.0 and sec[2] == 2.0 and sec[0] == 2.0
+    # runner-up: the largest value at any other index, NaN skipped, -inf if none;
+    # a tie for the maximum makes it equal to the maximum
+    assert sec.tolist() == [2.0, 5.0, 2.0, -inf, -inf, 0.5, -inf, 1.0, 1.0]
+    _, _, one = oracle_mod.argmax(np.array([[3.0], [nan]]))
+    assert one.tolist() == [-inf, -inf]
+
+
+def test_argmax_runner_up_matches_sorting(oracle_mod):
+    # against numpy: the runner-up is the second entry of the descending sort
+    # of the row's non-NaN fp32 values (duplicates kept)
+    r = np.random.default_rng(5)
+    rows = r.integers(-4, 5, size=(200, 7)).astype(np.float64) * 0.5
+    rows[r.random(rows.shape) < 0.1] = np.nan
+    idx, mx, sec = oracle_mod.argmax(rows)
+    for m in range(rows.shape[0]):
+        v = rows[m][~np.isnan(rows[m])].astype(np.float32)
+        if v.size == 0:
+            assert idx[m] == 0 and np.isnan(mx[m]) and sec[m] == -np.inf
+            continue
+        s = np.sort(v)[::-1]
+        assert mx[m] == s[0] and rows[m][idx[m]] == s[0]
+        assert sec[m] == (s[1] if s.size > 1 else -np.inf)
 
 
 # ---------------------------------------------------------------- accept walk
