@@ -13,7 +13,8 @@ stream, bracketed by a barrier and torch.cuda.synchronize(), CUDA events on
 that stream; the max over ranks is reported. The weights rotate over enough
 copies (11 x 50.5 MB = 555 MB) that every step reads them from HBM, not L2.
 `e2e` is the same metric through the public binding with the activations
-copied in from pinned host memory and the result copied back every step.
+copied in from pinned host memory and the result copied back every step, on
+one stream, timed on the host with one synchronization at the end.
 `--impl reference` times the CPU oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -312,31 +313,40 @@ def run_ours(args):
     achieved = b_main / per_launch / 1e9
     traffic = profiled_traffic("vq_linear_bf16_m%d_k5120_n17408" % Mr)
 
-    # ---- e2e through the public binding, host buffers, copies every step
-    x_host = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    x_host.copy_(x)
-    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    # ---- e2e through the public binding: every step copies its own x in from
+    # pinned host memory, runs vq_linear and copies its y back to pinned host
+    # memory, all on one stream (stream order sequences them); the host waits
+    # once, for the last step, at the end of the timed region
+    R = 16   # ring of host buffers: each in-flight step has its own input and output
+    x_host = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for _ in range(R)]
+    for h in x_host:
+        h.copy_(x)
+    y_host = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(R)]
     x_dev = torch.empty_like(x)
     e2e_steps = K_steps
-    for i in range(W):
-        x_dev.copy_(x_host, non_blocking=True)
+
+    def e2e_step(i):
+        x_dev.copy_(x_host[i % R], non_blocking=True)
         vq.vq_linear(x_dev, *copies[i % n_cp], y=y, workspace=ws)
-        y_host.copy_(y, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        y_host[i % R].copy_(y, non_blocking=True)
+
+    for i in range(W):
+        e2e_step(i)
+    torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for i in range(e2e_steps):
-        x_dev.copy_(x_host, non_blocking=True)
-        vq.vq_linear(x_dev, *copies[i % n_cp], y=y, workspace=ws)
-        y_host.copy_(y, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        e2e_step(i)
+    torch.cuda.current_stream().synchronize()
     t_e2e = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
     e2e = {"value": world * Mr * e2e_steps / t_e2e, "unit": "rows/s",
            "h2d_bytes_per_step": x.numel() * x.element_size(),
            "d2h_bytes_per_step": y.numel() * y.element_size(),
-           "us_per_step": t_e2e / e2e_steps * 1e6}
+           "us_per_step": t_e2e / e2e_steps * 1e6,
+           "method": "per step: pinned H2D of x, vq_linear, pinned D2H of y on one stream; "
+                     "host wall clock, one synchronization at the end"}
 
     line = {
         "metric": METRIC, "value": rows_per_s, "unit": "rows/s", "n_gpus": world,
@@ -434,7 +444,22 @@ def path_table(vq, copies, x, W, world):
     record("vocab_argmax_m64_k2560_n151936_bf16",
            [(lambda c=c: vq.vq_vocab_argmax(xv, *c, wsv, argmax=am)) for c in cv], bv, rows=Mv,
            n=100)
-    del cv
+    wst = torch.zeros(vq.vq_vocab_argmax_top2_workspace_bytes(Mv), dtype=torch.uint8,
+                      device="cuda")
+    record("vocab_argmax_top2_m64_k2560_n151936_bf16",
+           [(lambda c=c: vq.vq_vocab_argmax_top2(xv, *c, wst)) for c in cv], bv, rows=Mv, n=100)
+
+    # one fold-layout verify round (arg max -> accept -> commit of 8 layers x K,V)
+    case_r = synth.commit_case(0, keep=np.ones(4, dtype=np.int32))
+    kv_r = [torch.from_numpy(t.view(np.int16).copy()).cuda() for t in case_r.tensors]
+    i32r = lambda a: torch.from_numpy(np.asarray(a, dtype=np.int32)).cuda()
+    pl_r, so_r = i32r(case_r.prefix_len), i32r(case_r.src_off)
+    tok = torch.randint(0, Nv, (4, 16), dtype=torch.int32, device="cuda")
+    wsr = torch.zeros(vq.verify_round_workspace_bytes(4, 16), dtype=torch.uint8, device="cuda")
+    record("verify_round_b4_l16_k2560_n151936_8layers",
+           [(lambda c=c: vq.verify_round(xv, *c, tok, wsr, kv=kv_r, prefix_len=pl_r,
+                                         src_off=so_r)) for c in cv], bv, rows=Mv, n=100)
+    del cv, kv_r
 
     # accept walk B=4 x L=16 and the per-row KV commit (8 layers x K,V)
     tgt = torch.randint(0, Nv, (4, 16), dtype=torch.int32, device="cuda")

@@ -2,7 +2,8 @@
  * vq.h -- C ABI of the GB300 (sm_103a) block-verification hot path.
  *
  * Four operations make up one verify round of DFlash-style block speculative
- * decoding once the target has produced its hidden states:
+ * decoding once the target has produced its hidden states (verify_round
+ * chains the last three in one call):
  *
  *   vq_linear            the small-M verification projection over 4-bit
  *                        group-quantized weights
@@ -219,6 +220,45 @@ int kv_compact_per_row(void* const* tensors, int n_tensors, int B, int H, int S_
                        int elem_bytes, const int32_t* prefix_len, const int32_t* src_off,
                        const int32_t* keep, int max_keep, int32_t* new_len, int32_t* status,
                        void* stream);
+
+/*
+ * One verify round in one call, in the fold layout: vocabulary arg max over
+ * the verify block, accept walk, and per-row KV commit, enqueued back to back
+ * on `stream` with no host round trip (the call can be captured in a CUDA
+ * graph as it is).
+ *
+ * Source: ds4 #778 "dspark: fold first-token forward into verify ...", PR
+ * description and commit 1 (the committed token is verified as row 0 of the
+ * verify block, so one batched pass covers it and the drafts); mlxcel #2865,
+ * Summary (per-row accepts and the per-row KV commit).
+ *
+ *   tokens[b][0]      row b's committed token; tokens[b][1..L-1] its drafts
+ *   target[b][j]      = arg max of logits of verify row (b, j), as
+ *                       vq_vocab_argmax with M = B*L rows ordered (b, j)
+ *   accept[b]         = number of leading j in 0..L-2 with
+ *                       tokens[b][j+1] == target[b][j]   (0..L-1)
+ *   bonus[b]          = target[b][accept[b]]: the next block's committed token
+ *   KV commit         as kv_compact_per_row with keep[b] = accept[b] + 1 (the
+ *                     committed token's slot and the accepted drafts'),
+ *                     max_keep = L; skipped when n_tensors == 0.
+ *
+ * h          [B*L][K] hidden states of the verify block (act_dtype), the
+ *            vocabulary projection's x; qw, scales, biases as vq_vocab_argmax.
+ * tokens     int32 [B][L]; target int32 [B][L]; accept, bonus int32 [B].
+ * kv_tensors ... status: as kv_compact_per_row (HOST array of device
+ *            pointers); all ignored when n_tensors == 0.
+ * workspace  verify_round_workspace_bytes(B, L) bytes, 16-byte aligned,
+ *            zero-filled before its first use; left zero-filled where needed.
+ * Sizes      1 <= B*L <= 64, K a positive multiple of 512, N >= 1. Every
+ *            argument is checked before the first launch.
+ */
+size_t verify_round_workspace_bytes(int B, int L);
+int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
+                 const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                 const int32_t* tokens, int32_t* target, int32_t* accept, int32_t* bonus,
+                 void* const* kv_tensors, int n_tensors, int H, int S_cap, int D, int elem_bytes,
+                 const int32_t* prefix_len, const int32_t* src_off, int32_t* new_len,
+                 int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /* A short description of a VQ_* code. Never NULL. */
 const char* vq_strerror(int code);

@@ -135,6 +135,25 @@ def argmax(logits: np.ndarray):
     return idx, mx, sec
 
 
+def fold_accept(tokens: np.ndarray, target: np.ndarray):
+    """Fold layout (ds4 #778, PR description: the committed token verified as
+    row 0 of its block): tokens[b][0] is the committed token, tokens[b][1..]
+    the drafts, target[b][j] the greedy token after position j. Draft j+1 is
+    accepted while it equals target[b][j], i.e. the accept walk of the drafts
+    against the targets of the rows before them. Returns (accept, bonus,
+    keep) with bonus = target[b][accept[b]] and keep = accept + 1."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    target = np.ascontiguousarray(target, dtype=np.int32)
+    B, L = tokens.shape
+    assert target.shape == (B, L) and L >= 1
+    if L == 1:
+        acc = np.zeros(B, dtype=np.int32)
+    else:
+        acc = accept_walk(tokens[:, 1:], target[:, :-1])
+    bonus = target[np.arange(B), acc].astype(np.int32)
+    return acc, bonus, (acc + 1).astype(np.int32)
+
+
 def accept_walk(draft: np.ndarray, target: np.ndarray) -> np.ndarray:
     lib = _load()
     draft = np.ascontiguousarray(draft, dtype=np.int32)

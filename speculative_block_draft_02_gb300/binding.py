@@ -32,6 +32,9 @@ SIGNATURES = {
     "vq_vocab_argmax_top2": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _S, _P]),
     "verify_accept_walk": (_I, [_P, _P, _I, _I, _P, _P]),
     "kv_compact_per_row": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
+    "verify_round_workspace_bytes": (_S, [_I, _I]),
+    "verify_round": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                          _I, _P, _P, _P, _P, _P, _S, _P]),
     "vq_strerror": (ctypes.c_char_p, [_I]),
     "vq_device_error": (_I, [_P, _I, _P]),
 }
@@ -172,6 +175,43 @@ def kv_compact_per_row(tensors, prefix_len, src_off, keep, max_keep: int, new_le
                                   max_keep, _ptr(new_len), _ptr(status), _stream(stream))
     _check(rc, "kv_compact_per_row")
     return new_len
+
+
+def verify_round_workspace_bytes(B: int, L: int) -> int:
+    return int(lib().verify_round_workspace_bytes(B, L))
+
+
+def verify_round(h, qw, scales, biases, tokens, workspace, kv=None, prefix_len=None, src_off=None,
+                 new_len=None, status=None, target=None, accept=None, bonus=None, stream=None):
+    """One fold-layout verify round: (target int32[B][L], accept int32[B], bonus int32[B],
+    new_len int32[B] or None). tokens is int32 [B][L] (row 0 of each block = the committed
+    token); kv, if given, is the list of [B][H][S_cap][D] cache tensors to commit."""
+    B, L = tokens.shape
+    M, K = h.shape
+    N = qw.shape[0]
+    dev = h.device
+    if target is None:
+        target = torch.empty((B, L), dtype=torch.int32, device=dev)
+    if accept is None:
+        accept = torch.empty(B, dtype=torch.int32, device=dev)
+    if bonus is None:
+        bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    if kv:
+        t0 = kv[0]
+        _, H, S_cap, D = t0.shape
+        arr = (ctypes.c_void_p * len(kv))(*[_ptr(t).value for t in kv])
+        if new_len is None:
+            new_len = torch.empty(B, dtype=torch.int32, device=dev)
+        kv_args = (ctypes.cast(arr, ctypes.c_void_p), len(kv), H, S_cap, D, t0.element_size(),
+                   _ptr(prefix_len), _ptr(src_off), _ptr(new_len), _ptr(status))
+    else:
+        kv_args = (None, 0, 0, 0, 0, 0, None, None, None, None)
+    rc = lib().verify_round(_ptr(h), B, L, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
+                            _ACT[h.dtype], _ptr(tokens), _ptr(target), _ptr(accept), _ptr(bonus),
+                            *kv_args, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream(stream))
+    _check(rc, "verify_round")
+    return target, accept, bonus, (new_len if kv else None)
 
 
 def vq_device_error(clear: bool = False, stream=None) -> int:

@@ -30,6 +30,39 @@ __global__ void accept_walk_kernel(const int32_t* __restrict__ draft,
   if (lane == 0) accept[row] = a;
 }
 
+// Fold layout (ds4 #778, PR description: the committed token is verified as
+// row 0 of the verify block): tokens[b][0] is row b's committed token,
+// tokens[b][1..L-1] its drafts, and target[b][j] the greedy token the target
+// predicts after position j. Draft j+1 is accepted while it equals
+// target[b][j]: accept[b] in 0..L-1, bonus[b] = target[b][accept[b]] (the
+// next block's committed token), keep[b] = accept[b] + 1 KV slots (the
+// committed token's and the accepted drafts').
+__global__ void fold_accept_kernel(const int32_t* __restrict__ tokens,
+                                   const int32_t* __restrict__ target, int B, int L,
+                                   int32_t* __restrict__ accept, int32_t* __restrict__ bonus,
+                                   int32_t* __restrict__ keep) {
+  const int row = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= B) return;
+  const int32_t* d = tokens + (size_t)row * L + 1;
+  const int32_t* t = target + (size_t)row * L;
+  int a = L - 1;
+  for (int j0 = 0; j0 < L - 1; j0 += 32) {
+    const int j = j0 + lane;
+    const bool miss = j < L - 1 && d[j] != t[j];
+    const unsigned mask = __ballot_sync(0xffffffffu, miss);
+    if (mask) {
+      a = j0 + __ffs(mask) - 1;
+      break;
+    }
+  }
+  if (lane == 0) {
+    accept[row] = a;
+    bonus[row] = t[a];
+    keep[row] = a + 1;
+  }
+}
+
 constexpr int kMaxKvTensors = 64;
 struct KvTensors {
   void* p[kMaxKvTensors];
@@ -79,29 +112,42 @@ extern "C" int verify_accept_walk(const int32_t* draft, const int32_t* target, i
   return cudaGetLastError() == cudaSuccess ? VQ_OK : VQ_ECUDA;
 }
 
-extern "C" int kv_compact_per_row(void* const* tensors, int n_tensors, int B, int H, int S_cap,
-                                  int D, int elem_bytes, const int32_t* prefix_len,
-                                  const int32_t* src_off, const int32_t* keep, int max_keep,
-                                  int32_t* new_len, int32_t* status, void* stream) {
+namespace {
+// Host checks of a KV commit; fills the tensor table.
+int kv_check(void* const* tensors, int n_tensors, int B, int H, int S_cap, int D, int elem_bytes,
+             const int32_t* prefix_len, const int32_t* src_off, const int32_t* keep,
+             int max_keep, int32_t* new_len, int32_t* status, KvTensors* tp) {
   if (!tensors || n_tensors < 1 || n_tensors > kMaxKvTensors) return VQ_EINVAL;
   if (B < 1 || H < 1 || S_cap < 1 || D < 1 || elem_bytes < 1 || max_keep < 0) return VQ_EINVAL;
   if (!prefix_len || !src_off || !keep || !new_len) return VQ_EINVAL;
   const long long slot_bytes = (long long)D * elem_bytes;
   if (slot_bytes % 16 != 0) return VQ_EALIGN;
-  const long long buf_bytes = (long long)max_keep * slot_bytes;
-  if (buf_bytes > 160 * 1024) return VQ_EUNSUPPORTED;
-  const long long blocks = (long long)n_tensors * B * H;
-  if (blocks > 0x7fffffffLL) return VQ_EINVAL;
-  KvTensors tp;
-  for (int i = 0; i < kMaxKvTensors; ++i) tp.p[i] = nullptr;
+  if ((long long)max_keep * slot_bytes > 160 * 1024) return VQ_EUNSUPPORTED;
+  if ((long long)n_tensors * B * H > 0x7fffffffLL) return VQ_EINVAL;
+  for (int i = 0; i < kMaxKvTensors; ++i) tp->p[i] = nullptr;
   for (int i = 0; i < n_tensors; ++i) {
     if (!tensors[i]) return VQ_EINVAL;
     if ((uintptr_t)tensors[i] & 15u) return VQ_EALIGN;
-    tp.p[i] = tensors[i];
+    tp->p[i] = tensors[i];
   }
   if (((uintptr_t)prefix_len | (uintptr_t)src_off | (uintptr_t)keep | (uintptr_t)new_len |
        (uintptr_t)status) & 3u)
     return VQ_EALIGN;
+  return VQ_OK;
+}
+}  // namespace
+
+extern "C" int kv_compact_per_row(void* const* tensors, int n_tensors, int B, int H, int S_cap,
+                                  int D, int elem_bytes, const int32_t* prefix_len,
+                                  const int32_t* src_off, const int32_t* keep, int max_keep,
+                                  int32_t* new_len, int32_t* status, void* stream) {
+  KvTensors tp;
+  const int rc = kv_check(tensors, n_tensors, B, H, S_cap, D, elem_bytes, prefix_len, src_off,
+                          keep, max_keep, new_len, status, &tp);
+  if (rc) return rc;
+  const long long slot_bytes = (long long)D * elem_bytes;
+  const long long buf_bytes = (long long)max_keep * slot_bytes;
+  const long long blocks = (long long)n_tensors * B * H;
   const size_t smem = (size_t)(buf_bytes > 0 ? buf_bytes : 16);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(kv_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -112,4 +158,52 @@ extern "C" int kv_compact_per_row(void* const* tensors, int n_tensors, int B, in
       tp, B, H, S_cap, (int)(slot_bytes / 16), prefix_len, src_off, keep, max_keep, new_len,
       status);
   return cudaGetLastError() == cudaSuccess ? VQ_OK : VQ_ECUDA;
+}
+
+extern "C" size_t vq_vocab_argmax_workspace_bytes(int M);
+extern "C" int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_t* qw,
+                               const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                               int32_t* argmax, float* maxval, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+extern "C" size_t verify_round_workspace_bytes(int B, int L) {
+  if (B < 1 || L < 1 || (long long)B * L > 64) return 0;
+  return vq_vocab_argmax_workspace_bytes(B * L) + (((size_t)B * 4 + 15) & ~(size_t)15);
+}
+
+extern "C" int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
+                            const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                            const int32_t* tokens, int32_t* target, int32_t* accept,
+                            int32_t* bonus, void* const* kv_tensors, int n_tensors, int H,
+                            int S_cap, int D, int elem_bytes, const int32_t* prefix_len,
+                            const int32_t* src_off, int32_t* new_len, int32_t* status,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || L < 1 || (long long)B * L > 64) return VQ_EINVAL;
+  if (!tokens || !target || !accept || !bonus) return VQ_EINVAL;
+  if (((uintptr_t)tokens | (uintptr_t)target | (uintptr_t)accept | (uintptr_t)bonus) & 3u)
+    return VQ_EALIGN;
+  const size_t need = verify_round_workspace_bytes(B, L);
+  if (!workspace || workspace_bytes < need) return VQ_EWORKSPACE;
+  if ((uintptr_t)workspace & 15u) return VQ_EALIGN;
+  const size_t wa = vq_vocab_argmax_workspace_bytes(B * L);
+  int32_t* keep = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wa);
+  KvTensors tp;
+  if (n_tensors > 0) {
+    // every argument is checked before the first launch
+    const int rc = kv_check(kv_tensors, n_tensors, B, H, S_cap, D, elem_bytes, prefix_len,
+                            src_off, keep, L, new_len, status, &tp);
+    if (rc) return rc;
+  }
+  int rc = vq_vocab_argmax(h, B * L, K, N, qw, scales, biases, act_dtype, target, nullptr,
+                           workspace, wa, stream);
+  if (rc) return rc;
+  const int threads = 128;
+  const unsigned blocks = (unsigned)(((long long)B * 32 + threads - 1) / threads);
+  fold_accept_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(tokens, target, B, L, accept,
+                                                                   bonus, keep);
+  if (cudaGetLastError() != cudaSuccess) return VQ_ECUDA;
+  if (n_tensors > 0)
+    return kv_compact_per_row(kv_tensors, n_tensors, B, H, S_cap, D, elem_bytes, prefix_len,
+                              src_off, keep, L, new_len, status, stream);
+  return VQ_OK;
 }

@@ -82,6 +82,16 @@ def test_host_validation_rejects_before_any_launch(vqlib):
     assert vqlib.vq_linear(P(0x1002), 8, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -2
     assert vqlib.vq_vocab_argmax(fake, 8, 512, 16, fake, fake, fake, 0, None, None, fake, 64,
                                  None) == -1
+    # verify_round: B*L <= 64, outputs required, workspace checked before any launch
+    assert vqlib.verify_round_workspace_bytes(4, 16) == 528 + 16
+    assert vqlib.verify_round_workspace_bytes(8, 9) == 0
+    rnd = lambda B, L, tok, ws, nb: vqlib.verify_round(
+        fake, B, L, 512, 100, fake, fake, fake, 0, tok, fake, fake, fake, None, 0, 0, 0, 0, 0,
+        None, None, None, None, ws, nb, None)
+    assert rnd(8, 9, fake, fake, 4096) == -1
+    assert rnd(4, 16, None, fake, 4096) == -1
+    assert rnd(4, 16, fake, None, 0) == -5
+    assert rnd(4, 16, fake, fake, 16) == -5
     # the top-2 call needs its runner-up output, 4-byte aligned
     assert vqlib.vq_vocab_argmax_top2(fake, 8, 512, 16, fake, fake, fake, 0, fake, None, None,
                                       fake, 1 << 20, None) == -1

@@ -427,3 +427,58 @@ def test_commit_then_next_block_verify():
     y = run_linear(x, w, "bf16")
     cols = _sample_cols(cfg["N"], 7, 60)
     assert_proj_close(y[:, cols], oracle_linear(x, w, "bf16", cols), "bf16")
+
+
+# ------------------------------------------------------------ one verify round
+
+
+@pytest.mark.parametrize("B,L,K,N,layers", [(4, 16, 512, 20000, 2), (1, 8, 512, 3000, 1),
+                                            (8, 8, 1024, 12000, 0), (2, 1, 512, 5000, 1)])
+def test_verify_round_fold_layout(B, L, K, N, layers):
+    """vocab arg max -> fold accept -> KV commit in one call, against the
+    oracle composed the same way: target = arg max of the oracle logits,
+    (accept, bonus, keep) = fold accept, then the per-row commit with keep."""
+    M = B * L
+    w = synth.w4_weights(B * 100 + L, N, K)
+    hx = synth.activations(B * 100 + L, M, K, "bf16", name="hidden")
+    logits = oracle_linear(hx, w, "bf16")
+    r_target, _, _ = oracle.argmax(logits)
+    r_target = r_target.reshape(B, L)
+    # committed token in column 0, then drafts against the targets of the rows before
+    r = np.random.default_rng(B + L)
+    tokens = np.empty((B, L), dtype=np.int32)
+    tokens[:, 0] = r.integers(0, N, size=B)
+    if L > 1:
+        tokens[:, 1:] = synth.drafts_from_target(B + L, r_target[:, :-1], N)
+    r_acc, r_bonus, r_keep = oracle.fold_accept(tokens, r_target)
+
+    h = to_dev_act(hx, "bf16")
+    qw, sc, bi = to_dev_weights(w)
+    ws = torch.zeros(vq.verify_round_workspace_bytes(B, L), dtype=torch.uint8, device="cuda")
+    tok = torch.from_numpy(tokens).cuda()
+    if layers:
+        case = synth.commit_case(B + L, layers=layers, B=B, H=2, S_cap=512, D=64, block=L,
+                                 prefix_lo=20, prefix_hi=400, keep=r_keep)
+        kv = _kv_to_dev(case.tensors)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        target, acc, bonus, new_len = vq.verify_round(
+            h, qw, sc, bi, tok, ws, kv=kv, prefix_len=i32(case.prefix_len),
+            src_off=i32(case.src_off), status=status)
+    else:
+        target, acc, bonus, new_len = vq.verify_round(h, qw, sc, bi, tok, ws)
+    torch.cuda.synchronize()
+    target = target.cpu().numpy()
+    assert check_argmax(target.reshape(-1), np.zeros(M, np.float32) + logits.max(axis=1),
+                        logits) == 0
+    assert np.array_equal(target, r_target)
+    assert np.array_equal(acc.cpu().numpy(), r_acc)
+    assert np.array_equal(bonus.cpu().numpy(), r_bonus)
+    assert not ws[: vq.vq_vocab_argmax_workspace_bytes(M)].any()
+    if layers:
+        ref = [t.copy() for t in case.tensors]
+        r_len, r_status = oracle.kv_compact(ref, case.prefix_len, case.src_off, r_keep, L)
+        assert int(status.item()) == r_status == 0
+        assert np.array_equal(new_len.cpu().numpy(), r_len)
+        for d, rr in zip(kv, ref):
+            assert np.array_equal(d.cpu().numpy(), rr.view(np.int16))

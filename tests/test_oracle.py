@@ -265,6 +265,26 @@ def test_argmax_runner_up_matches_sorting(oracle_mod):
 # ---------------------------------------------------------------- accept walk
 
 
+def test_fold_accept_hand_cases(oracle_mod):
+    # rows: [committed, d1, d2, d3] against target [t0, t1, t2, t3] (t_j follows position j)
+    tokens = np.array([[7, 10, 11, 99],      # d1 = t0, d2 = t1, d3 != t2 -> accept 2, bonus t2
+                       [7, 10, 11, 12],      # every draft accepted -> accept 3, bonus t3
+                       [7, 55, 11, 12],      # first draft misses -> accept 0, bonus t0
+                       [7, 10, 11, 12]])     # same drafts, other targets (below)
+    target = np.array([[10, 11, 12, 13],
+                       [10, 11, 12, 13],
+                       [10, 11, 12, 13],
+                       [10, 77, 12, 13]])    # t1 differs -> accept 1, bonus 77
+    acc, bonus, keep = oracle_mod.fold_accept(tokens, target)
+    assert acc.tolist() == [2, 3, 0, 1]
+    assert bonus.tolist() == [12, 13, 10, 77]
+    assert keep.tolist() == [3, 4, 1, 2]
+    # a block of one token: nothing to accept, the bonus is the target of row 0
+    acc, bonus, keep = oracle_mod.fold_accept(np.array([[5]]), np.array([[9]]))
+    assert acc.tolist() == [0] and bonus.tolist() == [9] and keep.tolist() == [1]
+
+
+
 def test_accept_walk_hand_cases(oracle_mod):
     big = 2 ** 31 - 1
     tgt = np.array([
