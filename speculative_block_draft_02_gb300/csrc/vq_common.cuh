@@ -203,12 +203,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "r"(addr), "n"(kOff));
   return v;
 }
-template <int kOff>
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(kOff));
-  return v;
-}
 
 // Calls f(std::integral_constant<int, I>{}) for I = 0 .. N-1, so that loop
 // indices can feed compile-time immediates (e.g. load offsets).

@@ -27,14 +27,22 @@
 //               registers and issues mma.sync m16n8k16 with the weights as
 //               the 16-row A operand and the M activation rows as the n8
 //               operand(s), then folds the group into fp32 totals.
-//               X_g[m] for every group of K is computed once per block from
-//               global x while the first stages are in flight, and kept in
-//               shared memory.
+//   x           comes one of three ways: (a) vq_linear with 16-bit x and
+//               M <= 8: per-stage slices of scaled fp16 fragments, group sums
+//               and -U terms, prepared once per call by vq_prep_kernel and
+//               copied in next to each stage's weights; (b) the arg max with
+//               16-bit x, M <= 8 and several row blocks per block: a per-block
+//               fp16 table of all of x; (c) otherwise x per stage by TMA and
+//               X_g[m] for every group of K computed once per block from
+//               global x while the first stages are in flight.
 //   producer    one lane streams each stage (128 rows x 512 k of packed
-//               codes, their scales and biases, and the matching x[M][512])
-//               from HBM with cp.async.bulk.tensor (TMA) into a D-deep ring
-//               of shared-memory stages, completion tracked by mbarriers.
-// Every weight byte crosses HBM exactly once per call, for all M rows.
+//               codes, their scales and biases, and the stage's x) from HBM
+//               with cp.async.bulk.tensor (TMA) into a D-deep ring of
+//               shared-memory stages, completion tracked by mbarriers. The
+//               first stages' weights are requested before griddepcontrol.wait,
+//               so a call overlaps the tail of the kernel before it.
+// Every weight byte crosses HBM exactly once per call, for all M rows. (16-bit
+// x with M > 16 runs on the tcgen05 kernel in vq_tc.cuh instead.)
 //
 // MMA row i (0..7) of a warp maps to weight row 2i and MMA row i+8 to weight
 // row 2i+1: with the 128-byte TMA swizzle this puts the four rows read by a
@@ -447,7 +455,7 @@ __device__ __forceinline__ void consume_stage(uint32_t sb, uint32_t xsb,
       // B fragments of rows m = 8mt + g for k = 16t + 8h + (0..7):
       // bx[mt][s'][0..1] = (x_{2s'}, x_{2s'+4}), (x_{2s'+1}, x_{2s'+5})
       uint32_t bx[MT][2][2];
-      uint32_t bxm[MT][2][2], bxl[MT][2][2];   // fp32 only: middle / low terms
+      [[maybe_unused]] uint32_t bxm[MT][2][2], bxl[MT][2][2];   // fp32 only: middle / low terms
       static_for<MT>([&](auto mc) {
         constexpr int mt = decltype(mc)::value;
         if constexpr (!kF32) {
