@@ -36,7 +36,8 @@
 //                      (store y, or the running arg max).
 // X_g for all of K sits in shared memory: written once per call by a small
 // kernel into the workspace and copied in (vq_linear), or summed by the fold
-// warps at block start from x (arg max, whose blocks take many units).
+// warps from each stage's x tile during the block's first unit (arg max,
+// whose blocks take many units).
 #pragma once
 
 #include "vq_gemm.cuh"
@@ -195,6 +196,32 @@ __device__ __forceinline__ float tc_group_sum(const void* x, int K, int m, int g
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     const uint4 v = __ldg(src + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if constexpr (ACT == VQ_F16) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+        s += f.x;
+        s += f.y;
+      } else {
+        s += __uint_as_float(w[i] << 16);
+        s += __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  }
+  return s;
+}
+
+// X_g[m] from a stage's x tile in shared memory: group j's row m is 128 bytes
+// at tile + (j*MP + m)*128, its 16-byte chunks 128B-swizzled (chunk c at
+// (c ^ (m & 7)) << 4). Rows past M arrive zero-filled. Fixed summation order.
+template <int ACT, int MP>
+__device__ __forceinline__ float tc_group_sum_smem(uint32_t tile, int j, int m) {
+  const uint32_t row = tile + (uint32_t)((j * MP + m) * 128);
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 v = lds128_at(row + (((uint32_t)c ^ (uint32_t)(m & 7)) << 4));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -520,13 +547,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool aborted = false;
     // x and every output may belong to the kernel before this one
     grid_wait_prerequisites();
-    if constexpr (ARGMAX) {
-      for (int e = ft; e < (p.K / 64) * MP; e += kTcFoldWarps * 32) {
-        const int g = e / MP, m = e - g * MP;
-        xs_tab[e] = m < p.M ? tc_group_sum<ACT>(p.x, p.K, m, g) : 0.f;
-      }
-      named_bar_sync(1, kTcFoldWarps * 32);
-    } else {
+    if constexpr (!ARGMAX) {
       if (!wait_or_abort(xs_bar, 0u, abort_flag, p.err)) aborted = true;
     }
     float run_v = 0.f, run_s = -INFINITY;
@@ -543,6 +564,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             !wait_or_abort(full_bar(slot), (uint32_t)(q / p.D) & 1u, abort_flag, p.err))
           aborted = true;
         const uint32_t sb = base + slot * p.stage_bytes;
+        if constexpr (ARGMAX) {
+          // the block's first unit fills the X_g table from each stage's x
+          // tile (one (group, row) pair per fold thread); later units reuse it
+          if (u == (int)blockIdx.x) {
+            if (!aborted && ft < 8 * MP) {
+              const int j = ft / MP, m = ft - j * MP;
+              xs_tab[(kt * 8 + j) * MP + m] = tc_group_sum_smem<ACT, MP>(sb + kTcOffX, j, m);
+            }
+            named_bar_sync(1, kTcFoldWarps * 32);
+          }
+        }
         uint4 sv = make_uint4(0u, 0u, 0u, 0u), bv = sv;
         if (!aborted) {
           sv = lds128_at(sb + kTcOffS + (uint32_t)nl * 16u);
