@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-path", action="store_true", help="skip the per-kernel path table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--vocab", action="store_true",
+                    help="time the vocabulary projection with the fused arg max instead "
+                         "(M=64 rows = B 4 x block 16, K=2560, N=151936)")
     ap.add_argument("--rows", type=int, default=M, choices=[8, 64],
                     help="rows of the timed verify projection: 8 (the headline block) or 64 "
                          "(the next-block verify GEMM, B=4 x block 16)")
@@ -388,6 +391,53 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_vocab(args):
+    """The vocabulary projection + fused arg max as the timed step (M=64,
+    K=2560, N=151936, bf16): one JSON line with its time and roofline."""
+    from speculative_block_draft_02_gb300 import binding as vq
+    from speculative_block_draft_02_gb300 import build
+
+    rank, world, local = dist_setup()
+    build.build()
+    vq.lib()
+    dev = torch.cuda.current_device()
+    K_steps, W = args.steps, max(3, args.warmup)
+    Kv, Nv, Mv = 2560, 151936, 64
+    bv = Kv * Nv // 2 + 4 * Nv * (Kv // 64) + Mv * Kv * 2 + Mv * 4
+    n_cp = n_copies_for(bv)
+    _, cv = dev_weights(0, n_cp, Nv, Kv)
+    _, xv = dev_act(0, Mv, Kv)
+    wsv = torch.zeros(vq.vq_vocab_argmax_workspace_bytes(Mv), dtype=torch.uint8, device="cuda")
+    am = torch.empty(Mv, dtype=torch.int32, device="cuda")
+    calls = [(lambda c=c: vq.vq_vocab_argmax(xv, *c, wsv, argmax=am)) for c in cv]
+    clocks = ClockSampler(dev)
+    total, per_launch = time_calls(calls, K_steps, W, world, per_graph=100)
+    clk = clocks.stop()
+    peak, peak_kind = measured_peaks()
+    achieved = bv / per_launch / 1e9
+    line = {
+        "metric": "vocab projection + fused arg max rows/s and HBM GB/s", "impl": "ours",
+        "value": world * Mv * K_steps / total, "unit": "rows/s", "n_gpus": world,
+        "steps": K_steps, "warmup": W, "ms_per_step": total / K_steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "vocab_argmax_b4_l16_k2560_n151936", "M": Mv, "K": Kv, "N": Nv,
+                   "l2": "inputs > L2: %d rotating weight copies" % n_cp},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": profiled_traffic("vq_vocab_argmax_bf16_m64_k2560_n151936"),
+                     "algorithmic_bytes": bv, "kernel": "vq_tc_kernel<bf16, MP=64, ARGMAX>",
+                     "us_per_launch": per_launch * 1e6},
+        "gpu_launches": K_steps, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def path_table(vq, copies, x, W, world):
     """Every other step of the hot path, each at its own workload, timed the
     same way (fewer launches): microseconds per launch and algorithmic GB/s."""
@@ -563,6 +613,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.vocab:
+        run_vocab(args)
     else:
         run_ours(args)
 
