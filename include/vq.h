@@ -90,7 +90,11 @@ extern "C" {
  *          the projection, which may start before the slices are done and
  *          waits for them.
  * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 512,
- *          N >= 1. Other K (multiples of 64) return VQ_EUNSUPPORTED.
+ *          N >= 1. Other K (multiples of 64) return VQ_EUNSUPPORTED, and so do
+ *          shapes whose shared-memory plan does not fit: K > 32768 with 8 < M
+ *          <= 16; with fp32 x and M > 16, K > 12800; with 16-bit x, M > 16 and
+ *          an N narrow enough that K is split (N < 9728 on 152 SMs), K > 16384
+ *          for M <= 32 and K > 6144 above. vq_plan() tells whether a shape runs.
  * Accumulation is fp32; each 64-wide group is accumulated from exact integer
  * codes and scaled once, so the only roundings are the fp32 sums and the
  * final cast.
@@ -118,7 +122,8 @@ int vq_linear(const void* x, int M, int K, int N, const uint32_t* qw, const uint
  *          aligned, zero-filled before its first use; every call leaves it
  *          zero-filled again.
  * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 512,
- *          1 <= N < 2^31.
+ *          1 <= N < 2^31; as vq_linear, K > 32768 with 8 < M <= 16 and
+ *          K > 9728 with fp32 x and M > 16 return VQ_EUNSUPPORTED.
  */
 size_t vq_vocab_argmax_workspace_bytes(int M);
 int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_t* qw,
@@ -259,6 +264,28 @@ int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
                  void* const* kv_tensors, int n_tensors, int H, int S_cap, int D, int elem_bytes,
                  const int32_t* prefix_len, const int32_t* src_off, int32_t* new_len,
                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The launch plan a projection or arg max call would use, computed on the
+ * host for a device with `sm_count` SMs (no device is touched): which kernel,
+ * how deep its shared-memory ring is, how K is split, the grid, and the
+ * shared memory and workspace it needs. For capacity planning and tests; the
+ * calls themselves use the current device's SM count.
+ */
+typedef struct {
+  int32_t kernel;       /* 0 mma.sync, x per stage; 1 mma.sync, per-block x table;
+                           2 mma.sync, prepared x slices; 3 tcgen05 */
+  int32_t rows_padded;  /* M rounded up to the kernel's row tile (8, 16, 32 or 64) */
+  int32_t stages;       /* depth of the shared-memory stage ring (512 k per stage) */
+  int32_t prefetch;     /* stages whose weights are requested before the wait */
+  int32_t k_splits;     /* K splits per 128-row block (1 = none) */
+  int32_t units;        /* 128-row blocks x K splits */
+  int32_t grid;         /* blocks launched (persistent over units) */
+  int32_t launches;     /* kernels per call */
+  int64_t smem_bytes;   /* dynamic shared memory per block */
+  int64_t workspace_bytes;
+} vq_plan_t;
+int vq_plan(int M, int K, int N, int act_dtype, int argmax, int sm_count, vq_plan_t* out);
 
 /* A short description of a VQ_* code. Never NULL. */
 const char* vq_strerror(int code);

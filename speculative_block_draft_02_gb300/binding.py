@@ -35,6 +35,7 @@ SIGNATURES = {
     "verify_round_workspace_bytes": (_S, [_I, _I]),
     "verify_round": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                           _I, _P, _P, _P, _P, _P, _S, _P]),
+    "vq_plan": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "vq_strerror": (ctypes.c_char_p, [_I]),
     "vq_device_error": (_I, [_P, _I, _P]),
 }
@@ -212,6 +213,21 @@ def verify_round(h, qw, scales, biases, tokens, workspace, kv=None, prefix_len=N
                             _stream(stream))
     _check(rc, "verify_round")
     return target, accept, bonus, (new_len if kv else None)
+
+
+class _Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("kernel", "rows_padded", "stages", "prefetch",
+                                               "k_splits", "units", "grid", "launches")] + \
+               [("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+
+def vq_plan(M: int, K: int, N: int, act=torch.bfloat16, argmax: bool = False,
+            sm_count: int = 152) -> dict:
+    """The launch plan of a projection (or arg max) call, computed on the host."""
+    p = _Plan()
+    _check(lib().vq_plan(M, K, N, _ACT[act], int(argmax), sm_count,
+                         ctypes.cast(ctypes.byref(p), ctypes.c_void_p)), "vq_plan")
+    return {n: getattr(p, n) for n, _ in _Plan._fields_}
 
 
 def vq_device_error(clear: bool = False, stream=None) -> int:

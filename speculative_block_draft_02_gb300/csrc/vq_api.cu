@@ -107,7 +107,7 @@ int red_bytes(int MT) {
 struct Plan {
   int MT, MP, D, pre, KT, RB, S, n_units, grid;
   bool red_alias;   // K-slice partials in the stage ring (one unit per block)
-  int stage_bytes, off_x, off_s, off_b, xbox_bytes, xm, tab_bytes;
+  int stage_bytes, off_x, off_s, off_b, xbox_bytes, xm, tab_bytes, xs_stage;
   uint32_t tx_bytes;
   size_t smem;
   size_t ws_xp_bytes;    // prepared x table (start of the workspace), 0 if none
@@ -161,8 +161,15 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   //         (25.7 vs 20.6 us), its per-group MMA issue and handoffs cost more
   //         than the 16-row mma.sync work they replace.
   if (!f32 && p.MT >= 4 && p.S == 1) {
-    const int tab_tc = (int)round_up((size_t)tc_xs_bytes(K, p.MP), 1024);
+    // a table of X_g for all of K if it leaves room for two stages, else
+    // X_g per stage from the x tile (two stages' worth, double-buffered)
     const int sb = tc_stage_bytes(p.MP);
+    int tab_tc = (int)round_up((size_t)tc_xs_bytes(K, p.MP), 1024);
+    p.xs_stage = 0;
+    if ((kSmemLimit - 1024 - kTcMiscBytes - tab_tc) / sb < 2) {
+      p.xs_stage = 1;
+      tab_tc = (int)round_up((size_t)2 * 8 * p.MP * 4, 1024);
+    }
     int D = (kSmemLimit - 1024 - kTcMiscBytes - tab_tc) / sb;
     if (D > kMaxStages) D = kMaxStages;
     if (D >= 2) {
@@ -183,7 +190,7 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
         p.ws_xp_bytes = 0;
         p.ws_bytes = round_up((size_t)M * 8 + 4, 16);
       } else {
-        p.ws_xp_bytes = round_up((size_t)tc_xs_bytes(K, p.MP), 256);
+        p.ws_xp_bytes = p.xs_stage ? 0 : round_up((size_t)tc_xs_bytes(K, p.MP), 256);
         p.ws_bytes = p.ws_xp_bytes;
       }
       *pl = p;
@@ -309,6 +316,7 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
 
   p.tx_bytes = pl.tx_bytes;
   p.xm = pl.xm;
+  p.xs_stage = pl.xs_stage;
   p.tab_bytes = pl.tab_bytes;
   p.y = y;
   p.err = err;
@@ -407,6 +415,25 @@ extern "C" int vq_vocab_argmax(const void* x, int M, int K, int N, const uint32_
                                size_t workspace_bytes, void* stream) {
   return run_gemm(x, M, K, N, qw, scales, biases, act_dtype, true, nullptr, argmax, maxval,
                   workspace, workspace_bytes, stream);
+}
+
+extern "C" int vq_plan(int M, int K, int N, int act_dtype, int argmax, int sm_count,
+                       vq_plan_t* out) {
+  if (!out || sm_count < 1) return VQ_EINVAL;
+  Plan pl;
+  const int rc = make_plan(M, K, N, act_dtype, argmax != 0, sm_count, &pl);
+  if (rc) return rc;
+  out->kernel = pl.xm;
+  out->rows_padded = pl.MP;
+  out->stages = pl.D;
+  out->prefetch = pl.pre;
+  out->k_splits = pl.S;
+  out->units = pl.n_units;
+  out->grid = pl.grid;
+  out->launches = (pl.xm == 2 || (pl.xm == 3 && !argmax && !pl.xs_stage)) ? 2 : 1;
+  out->smem_bytes = (int64_t)pl.smem;
+  out->workspace_bytes = (int64_t)pl.ws_bytes;
+  return VQ_OK;
 }
 
 extern "C" size_t vq_vocab_argmax_top2_workspace_bytes(int M) {

@@ -156,6 +156,8 @@ struct GemmParams {
   int off_x, off_s, off_b;   // offsets inside a stage (codes at 0)
   int xm;           // x source: 0 per-stage TMA, 1 per-block table, 2 prepared slices,
                     // 3 per-stage TMA for the tensor-core (tcgen05) kernel
+  int xs_stage;     // tcgen05 kernel: 1 = group row sums per stage from the x tile,
+                    // 0 = a table for all of K
   const void* xprep;  // prepared slices [KT] (xm == 2), written by vq_prep_kernel
   int tab_bytes;    // bytes of the table region after the stage ring (1 KiB multiple)
   int x3d;          // 1: x arrives as one 3-D box per stage, 0: one box per group

@@ -34,10 +34,12 @@
 //                      warp) and the fp32
 //                      fold with scale, bias and X_g; then the epilogue
 //                      (store y, or the running arg max).
-// X_g for all of K sits in shared memory: written once per call by a small
-// kernel into the workspace and copied in (vq_linear), or summed by the fold
-// warps from each stage's x tile during the block's first unit (arg max,
-// whose blocks take many units).
+// X_g: a table for all of K in shared memory, written once per call by a
+// small kernel into the workspace and copied in (vq_linear), or summed by the
+// fold warps from each stage's x tile during the block's first unit (arg max,
+// whose blocks take many units); when the table would leave room for fewer
+// than two stages (long K at M > 32), the fold warps sum each stage's groups
+// from its x tile into a double-buffered area instead, and K is not limited.
 #pragma once
 
 #include "vq_gemm.cuh"
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++pre;
         }
       grid_wait_prerequisites();
-      if constexpr (!ARGMAX) {
+      if (!ARGMAX && !p.xs_stage) {
         const uint32_t xs_bytes = (uint32_t)tc_xs_bytes(p.K, MP);
         mbar_arrive_expect_tx(xs_bar, xs_bytes);
         bulk_load(smem_addr(xs_tab), p.xprep, xs_bytes, xs_bar);
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // let every copy issued land before the block can exit
       for (int r = (q > p.D ? q - p.D : 0); r < q; ++r)
         wait_bounded(full_bar(r % p.D), (uint32_t)(r / p.D) & 1u, p.err);
-      if constexpr (!ARGMAX) wait_bounded(xs_bar, 0u, p.err);
+      if (!ARGMAX && !p.xs_stage) wait_bounded(xs_bar, 0u, p.err);
     }
   } else if (warp >= kTcMmaWarp) {
     // ------------------------------------------------------------- MMA issue
@@ -547,7 +549,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bool aborted = false;
     // x and every output may belong to the kernel before this one
     grid_wait_prerequisites();
-    if constexpr (!ARGMAX) {
+    if (!ARGMAX && !p.xs_stage) {
       if (!wait_or_abort(xs_bar, 0u, abort_flag, p.err)) aborted = true;
     }
     float run_v = 0.f, run_s = -INFINITY;
@@ -564,16 +566,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             !wait_or_abort(full_bar(slot), (uint32_t)(q / p.D) & 1u, abort_flag, p.err))
           aborted = true;
         const uint32_t sb = base + slot * p.stage_bytes;
-        if constexpr (ARGMAX) {
-          // the block's first unit fills the X_g table from each stage's x
-          // tile (one (group, row) pair per fold thread); later units reuse it
-          if (u == (int)blockIdx.x) {
-            if (!aborted && ft < 8 * MP) {
-              const int j = ft / MP, m = ft - j * MP;
-              xs_tab[(kt * 8 + j) * MP + m] = tc_group_sum_smem<ACT, MP>(sb + kTcOffX, j, m);
-            }
-            named_bar_sync(1, kTcFoldWarps * 32);
+        // X_g of this stage's groups: from the table, or summed here from the
+        // stage's x tile (one (group, row) pair per fold thread) into a
+        // double-buffered area (per-stage mode, or the arg max's first unit,
+        // which fills the table for the units after it)
+        const float* xs_base = xs_tab + kt * 8 * MP;
+        if (p.xs_stage || (ARGMAX && u == (int)blockIdx.x)) {
+          float* dst = p.xs_stage ? xs_tab + (q & 1) * 8 * MP : xs_tab + kt * 8 * MP;
+          if (!aborted && ft < 8 * MP) {
+            const int j = ft / MP, m = ft - j * MP;
+            dst[j * MP + m] = tc_group_sum_smem<ACT, MP>(sb + kTcOffX, j, m);
           }
+          named_bar_sync(1, kTcFoldWarps * 32);
+          xs_base = dst;
         }
         uint4 sv = make_uint4(0u, 0u, 0u, 0u), bv = sv;
         if (!aborted) {
@@ -612,8 +617,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float s = __uint_as_float(h ? (s2 & 0xFFFF0000u) : (s2 << 16));
               const float bb = __uint_as_float(h ? (b2 & 0xFFFF0000u) : (b2 << 16));
               const float c = fmaf(-kC0, s, bb);   // exact: bias - c0*scale
-              const float4* xs4 =
-                  reinterpret_cast<const float4*>(xs_tab + (kt * 8 + j) * MP + HC * ch);
+              const float4* xs4 = reinterpret_cast<const float4*>(xs_base + j * MP + HC * ch);
               const uint32_t* acc = h ? acc1 : acc0;
 #pragma unroll
               for (int i4 = 0; i4 < HC / 4; ++i4) {
@@ -709,7 +713,7 @@ int launch_tc(const GemmLaunch& L) {
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem) !=
       cudaSuccess)
     return VQ_ECUDA;
-  if constexpr (!AM) {
+  if (!AM && !L.p.xs_stage) {
     const int n = (L.p.K / 64) * MP;
     const int rc = launch_pdl(vq_tc_xsum_kernel<ACT>, dim3((n + 255) / 256), 256, 0, L.stream,
                               L.p.x, L.p.M, L.p.K, MP, (float*)L.p.xprep);

@@ -113,6 +113,27 @@ def test_linear_tensor_core_path(M, K, N, dtype):
     assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
 
 
+# long K on the tcgen05 kernel: the group row sums are taken per stage from
+# the x tile (a table for all of K would not fit beside two stages)
+@pytest.mark.parametrize("M,K,N,dtype", [(64, 8192, 9800, "bf16"), (40, 17408, 9728, "f16")])
+def test_linear_tensor_core_long_k(M, K, N, dtype):
+    seed = 11 * M + K
+    w = synth.w4_weights(seed, N, K)
+    x = synth.activations(seed, M, K, dtype)
+    y = run_linear(x, w, dtype)
+    cols = _sample_cols(N, 9, 150)
+    assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
+
+
+def test_vocab_argmax_tensor_core_long_k():
+    M, K, N = 64, 8192, 12000
+    w = synth.w4_weights(77, N, K)
+    x = synth.activations(77, M, K, "bf16")
+    idx, mx, ws = run_vocab(x, w)
+    check_argmax(idx, mx, oracle_linear(x, w, "bf16"))
+    assert not ws.any()
+
+
 @pytest.mark.parametrize("M,K,N,dtype", [(17, 512, 3000, "bf16"), (20, 1024, 9000, "f16"),
                                          (64, 1024, 40000, "f16")])
 def test_vocab_argmax_tensor_core_path(M, K, N, dtype):
