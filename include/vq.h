@@ -270,7 +270,10 @@ int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
  * host for a device with `sm_count` SMs (no device is touched): which kernel,
  * how deep its shared-memory ring is, how K is split, the grid, and the
  * shared memory and workspace it needs. For capacity planning and tests; the
- * calls themselves use the current device's SM count.
+ * calls themselves use the current device's SM count. The pages have no
+ * counterpart: this reports how this library maps a shape onto the GPU.
+ * Returns VQ_OK and fills *out, or the code the call itself would return for
+ * this shape (VQ_EINVAL, VQ_EUNSUPPORTED); out must be a host pointer.
  */
 typedef struct {
   int32_t kernel;       /* 0 mma.sync, x per stage; 1 mma.sync, per-block x table;
