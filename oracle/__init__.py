@@ -17,6 +17,9 @@ and which passage of the pages it follows, is stated in the C file:
   (mlxcel #2865, Summary).
 * ``kv_compact``  -- per-row KV commit to a contiguous valid prefix
   (mlxcel #2865, Summary).
+* ``verify_attention`` -- the verify block's attention at each row's logical
+  positions with the stale gap masked (mlxcel #2865, Summary and commit
+  message), with ``round_bits`` its rounding to the 16-bit storage formats.
 """
 from __future__ import annotations
 
@@ -70,6 +73,12 @@ def _load():
             lib.oracle_bf16_to_double.restype = ctypes.c_double
             lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
             lib.oracle_f16_to_double.restype = ctypes.c_double
+            lib.oracle_round_bits.argtypes = [ctypes.c_double, i]
+            lib.oracle_round_bits.restype = ctypes.c_uint16
+            lib.oracle_verify_attention.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i,
+                                                    ctypes.c_double, ctypes.c_double, i, p, p,
+                                                    p, i]
+            lib.oracle_verify_attention.restype = i
             lib.oracle_num_threads.argtypes = []
             lib.oracle_num_threads.restype = i
             _lib = lib
@@ -190,3 +199,38 @@ def bf16_to_double(h: int) -> float:
 
 def f16_to_double(h: int) -> float:
     return _load().oracle_f16_to_double(h)
+
+
+def round_bits(v: float, dtype: int) -> int:
+    """Bits of v rounded to bf16 (dtype 0) or f16 (dtype 1), nearest even."""
+    return int(_load().oracle_round_bits(float(v), dtype))
+
+
+def verify_attention(q, k_new, v_new, k_cache, v_cache, prefix_len, src_off, dtype: int,
+                     rotary_dim: int, theta: float, scale: float, threads: int | None = None):
+    """Verify-block attention; k_cache / v_cache are updated in place.
+
+    q [B][L][Hq][D], k_new / v_new [B][L][Hkv][D], caches [B][Hkv][S_cap][D]: uint16
+    bits of dtype (0 bf16, 1 f16). Returns (out fp64 [B][L][Hq][D], k_rot fp64
+    [B][L][Hkv][D] before rounding, status).
+    """
+    lib = _load()
+    B, L, Hq, D = q.shape
+    Hkv = k_new.shape[2]
+    S_cap = k_cache.shape[2]
+    arrs = [np.ascontiguousarray(a, dtype=np.uint16) for a in (q, k_new, v_new)]
+    assert arrs[1].shape == arrs[2].shape == (B, L, Hkv, D)
+    for c in (k_cache, v_cache):
+        assert c.dtype == np.uint16 and c.flags["C_CONTIGUOUS"] and c.shape == (B, Hkv, S_cap, D)
+    pl = np.ascontiguousarray(prefix_len, dtype=np.int32)
+    so = np.ascontiguousarray(src_off, dtype=np.int32)
+    out = np.empty((B, L, Hq, D), dtype=np.float64)
+    k_rot = np.empty((B, L, Hkv, D), dtype=np.float64)
+    status = np.zeros(1, dtype=np.int32)
+    rc = lib.oracle_verify_attention(_ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(pl), _ptr(so), B, L, Hq, Hkv, D, S_cap,
+                                     rotary_dim, float(theta), float(scale), dtype, _ptr(out),
+                                     _ptr(k_rot), _ptr(status), threads or num_threads())
+    if rc != 0:
+        raise ValueError("oracle_verify_attention rejected its arguments")
+    return out, k_rot, int(status[0])

@@ -256,3 +256,201 @@ void oracle_kv_compact(void **tensors, int n_tensors, int B, int H, int S_cap, i
     if (status) *status = st;
     free(tmp);
 }
+
+/*
+ * Rounding to a 16-bit storage format, to nearest with ties to even.
+ *
+ * A binary format with `frac` fraction bits and smallest normal exponent emin
+ * holds, in the binade [2^e, 2^(e+1)), the multiples of 2^(e - frac); below
+ * 2^emin (the subnormals) the multiples of 2^(emin - frac). v / spacing is
+ * exact in double (a power-of-two scaling), so rint() (ties to even in the
+ * default rounding mode) picks the nearest representable neighbour. A
+ * magnitude that rounds above the largest finite value becomes infinite.
+ *   binary16: frac 10, emin -14, largest finite 65504
+ *   bfloat16: frac 7,  emin -126, largest finite (2 - 2^-7) * 2^127
+ */
+static double round_to_format(double v, int frac, int emin, double max_finite)
+{
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    int e;
+    frexp(fabs(v), &e);            /* |v| = f * 2^e, f in [0.5, 1): leading bit 2^(e-1) */
+    int lead = e - 1;
+    if (lead < emin) lead = emin;
+    double spacing = ldexp(1.0, lead - frac);
+    double r = rint(v / spacing) * spacing;
+    if (fabs(r) > max_finite) return v > 0 ? INFINITY : -INFINITY;
+    return r;
+}
+
+static double round_to_storage(double v, int dtype)
+{
+    if (dtype == ORACLE_BF16) return round_to_format(v, 7, -126, ldexp(2.0 - ldexp(1.0, -7), 127));
+    return round_to_format(v, 10, -14, 65504.0);
+}
+
+/* Bits of a value that is already representable in the storage format. */
+static uint16_t storage_bits(double r, int dtype)
+{
+    if (dtype == ORACLE_BF16) {
+        float f = (float)r;                       /* exact: bf16 values are binary32 values */
+        uint32_t u;
+        memcpy(&u, &f, sizeof u);
+        return (uint16_t)(u >> 16);
+    }
+    uint16_t sign = signbit(r) ? 0x8000u : 0u;
+    double a = fabs(r);
+    if (isnan(r)) return 0x7E00u;
+    if (isinf(r)) return (uint16_t)(sign | 0x7C00u);
+    if (a < ldexp(1.0, -14))                      /* zero or subnormal: a = f * 2^-24 */
+        return (uint16_t)(sign | (uint16_t)(a * ldexp(1.0, 24)));
+    int e;
+    frexp(a, &e);
+    int lead = e - 1;                             /* a = (1 + m/1024) * 2^lead */
+    uint16_t m = (uint16_t)((ldexp(a, -lead) - 1.0) * 1024.0);
+    return (uint16_t)(sign | (uint16_t)((lead + 15) << 10) | m);
+}
+
+static double storage_to_double(uint16_t h, int dtype)
+{
+    return dtype == ORACLE_BF16 ? bf16_bits_to_double(h) : f16_bits_to_double(h);
+}
+
+/* Exposed so the tests can pin the rounding against library conversions. */
+uint16_t oracle_round_bits(double v, int dtype) { return storage_bits(round_to_storage(v, dtype), dtype); }
+
+/*
+ * Rotary position embedding of one head vector at position `pos`, in the
+ * half-split pairing: within the first rotary_dim dimensions, dimension i
+ * (i < rotary_dim/2) pairs with i + rotary_dim/2, and the pair turns by the
+ * angle pos * theta^(-2i / rotary_dim):
+ *     y[i]        = x[i] cos a - x[i + h] sin a
+ *     y[i + h]    = x[i + h] cos a + x[i] sin a        (h = rotary_dim / 2)
+ * Dimensions rotary_dim .. D-1 pass through.
+ */
+static void rope_vector(const double *x, double *y, int D, int rotary_dim, double pos,
+                        double theta)
+{
+    int h = rotary_dim / 2;
+    for (int i = 0; i < h; ++i) {
+        double a = pos * pow(theta, -2.0 * (double)i / (double)rotary_dim);
+        double c = cos(a), s = sin(a);
+        y[i] = x[i] * c - x[i + h] * s;
+        y[i + h] = x[i + h] * c + x[i] * s;
+    }
+    for (int d = rotary_dim; d < D; ++d) y[d] = x[d];
+}
+
+/*
+ * Verify-block attention over the per-row cache (mlxcel #2865 "perf(speculative):
+ * commit per-row accepts in batched DFlash", Summary and commit message: once each
+ * row keeps its own accept count, the verify block is rotated and attends at every
+ * row's own logical positions, and the stale gap between the row's valid prefix and
+ * the shared verify slots is masked for every query).
+ *
+ * Layouts (16-bit storage, dtype bf16 or f16 for every tensor):
+ *   q         [B][L][Hq][D]   the verify block's queries, before rotation
+ *   k_new     [B][L][Hkv][D]  its keys, before rotation;  v_new the same for values
+ *   k_cache, v_cache [B][Hkv][S_cap][D]: row b holds its valid prefix in slots
+ *             0 .. prefix_len[b]-1 (keys stored rotated), and the verify block is
+ *             appended at slots src_off[b] .. src_off[b]+L-1.
+ * For each row b (P = prefix_len[b], S = src_off[b]) and block position j:
+ *   1. the logical position of the block's token j is P + j; its key is rotated
+ *      there, rounded to the storage format and written to slot S + j of k_cache,
+ *      and its value is copied to slot S + j of v_cache;
+ *   2. its query (head hq, kv head hq / (Hq / Hkv)) is rotated at P + j and rounded
+ *      to the storage format;
+ *   3. it attends, with softmax(scale * q.k), to the cache slots 0 .. P-1 and to the
+ *      block's slots S .. S + j (causal within the block); slots P .. S-1, the stale
+ *      gap, and everything after S + j are masked out.
+ * out      [B][L][Hq][D] fp64, unrounded.
+ * k_rot    optional [B][L][Hkv][D] fp64: the rotated keys before rounding.
+ * A row with P < 0, S < P or S + L > S_cap is left untouched in the caches, gets
+ * zero outputs, and sets bit 0 of *status (status optional).
+ * Returns 0, or -1 on a shape the definition does not cover.
+ */
+int oracle_verify_attention(const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                            uint16_t *k_cache, uint16_t *v_cache, const int32_t *prefix_len,
+                            const int32_t *src_off, int B, int L, int Hq, int Hkv, int D,
+                            int S_cap, int rotary_dim, double theta, double scale, int dtype,
+                            double *out, double *k_rot, int32_t *status, int n_threads)
+{
+    if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || S_cap < L) return -1;
+    if (rotary_dim < 0 || rotary_dim > D || rotary_dim % 2 != 0) return -1;
+    if (dtype != ORACLE_BF16 && dtype != ORACLE_F16) return -1;
+    const int G = Hq / Hkv;
+    int32_t st = 0;
+    memset(out, 0, sizeof(double) * (size_t)B * L * Hq * D);
+    if (k_rot) memset(k_rot, 0, sizeof(double) * (size_t)B * L * Hkv * D);
+
+    double *xv = (double *)malloc(sizeof(double) * (size_t)D);
+    double *yv = (double *)malloc(sizeof(double) * (size_t)D);
+    for (int b = 0; b < B; ++b) {
+        int P = prefix_len[b], S = src_off[b];
+        if (P < 0 || S < P || S + L > S_cap) {
+            st |= 1;
+            continue;
+        }
+        /* step 1: the block's keys and values go to slots S .. S+L-1 */
+        for (int j = 0; j < L; ++j)
+            for (int h = 0; h < Hkv; ++h) {
+                size_t src = (((size_t)b * L + j) * Hkv + h) * D;
+                size_t dst = (((size_t)b * Hkv + h) * S_cap + (size_t)(S + j)) * D;
+                for (int d = 0; d < D; ++d) xv[d] = storage_to_double(k_new[src + d], dtype);
+                rope_vector(xv, yv, D, rotary_dim, (double)(P + j), theta);
+                for (int d = 0; d < D; ++d) {
+                    if (k_rot) k_rot[src + d] = yv[d];
+                    k_cache[dst + d] = storage_bits(round_to_storage(yv[d], dtype), dtype);
+                    v_cache[dst + d] = v_new[src + d];
+                }
+            }
+    }
+    free(xv);
+    free(yv);
+
+    /* steps 2 and 3, one query (b, j, hq) at a time */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(dynamic) num_threads(n_threads > 0 ? n_threads : 1)
+#endif
+    for (long long qi = 0; qi < (long long)B * L * Hq; ++qi) {
+        int hq = (int)(qi % Hq);
+        int j = (int)((qi / Hq) % L);
+        int b = (int)(qi / ((long long)Hq * L));
+        int P = prefix_len[b], S = src_off[b];
+        if (P < 0 || S < P || S + L > S_cap) continue;
+        int hk = hq / G;
+        int n_vis = P + j + 1;
+        double *qv = (double *)malloc(sizeof(double) * (size_t)D * 2);
+        double *sc = (double *)malloc(sizeof(double) * (size_t)n_vis);
+        size_t qoff = (size_t)qi * D;     /* [B][L][Hq][D] flattened in the same order */
+        for (int d = 0; d < D; ++d) qv[D + d] = storage_to_double(q[qoff + d], dtype);
+        rope_vector(qv + D, qv, D, rotary_dim, (double)(P + j), theta);
+        for (int d = 0; d < D; ++d) qv[d] = round_to_storage(qv[d], dtype);
+
+        const uint16_t *kb = k_cache + ((size_t)b * Hkv + hk) * (size_t)S_cap * D;
+        const uint16_t *vb = v_cache + ((size_t)b * Hkv + hk) * (size_t)S_cap * D;
+        /* visible slot number t: the prefix slot t for t < P, else the block slot S + (t - P) */
+        double mx = -INFINITY;
+        for (int t = 0; t < n_vis; ++t) {
+            size_t slot = (size_t)(t < P ? t : S + (t - P));
+            double dot = 0.0;
+            for (int d = 0; d < D; ++d) dot += qv[d] * storage_to_double(kb[slot * D + d], dtype);
+            sc[t] = scale * dot;
+            if (sc[t] > mx) mx = sc[t];
+        }
+        double l = 0.0;
+        for (int t = 0; t < n_vis; ++t) {
+            sc[t] = exp(sc[t] - mx);
+            l += sc[t];
+        }
+        double *o = out + qoff;
+        for (int t = 0; t < n_vis; ++t) {
+            size_t slot = (size_t)(t < P ? t : S + (t - P));
+            for (int d = 0; d < D; ++d) o[d] += sc[t] * storage_to_double(vb[slot * D + d], dtype);
+        }
+        for (int d = 0; d < D; ++d) o[d] /= l;
+        free(qv);
+        free(sc);
+    }
+    if (status) *status = st;
+    return 0;
+}

@@ -145,7 +145,46 @@ def commit_case(seed: int, layers: int = 8, B: int = 4, H: int = 8, S_cap: int =
                       np.asarray(keep, dtype=np.int32), block)
 
 
-# The five seeded workloads, by what they are. Seed 0 throughout.
+@dataclass
+class AttentionCase:
+    q: np.ndarray            # uint16 bits [B][L][Hq][D]
+    k_new: np.ndarray        # uint16 bits [B][L][Hkv][D]
+    v_new: np.ndarray        # uint16 bits [B][L][Hkv][D]
+    k_cache: np.ndarray      # uint16 bits [B][Hkv][S_cap][D]
+    v_cache: np.ndarray      # uint16 bits [B][Hkv][S_cap][D]
+    prefix_len: np.ndarray   # int32 [B]
+    src_off: np.ndarray      # int32 [B]
+    dtype: str
+
+
+def attention_case(seed: int, B: int = 4, L: int = 16, Hq: int = 32, Hkv: int = 8,
+                   D: int = 128, S_cap: int = 2048, prefix_lo: int = 200,
+                   prefix_hi: int = 1800, dtype: str = "f16", src_off=None, prefix_len=None,
+                   name: str = "attn") -> AttentionCase:
+    """The verify block's attention inputs over a rectangular cache.
+
+    q, k_new, v_new and every cache slot (the valid prefix, the stale gap and the
+    unused tail alike) ~ N(0, 1) in `dtype`. prefix_len ~ U{prefix_lo..prefix_hi}
+    unless given; the verify block sits at the shared offset max prefix_len (the
+    rectangular cache) unless src_off is given.
+    """
+    if prefix_len is None:
+        prefix_len = rng_for(seed, name + ".lens").integers(prefix_lo, prefix_hi + 1, size=B)
+    prefix_len = np.asarray(prefix_len, dtype=np.int32)
+    if src_off is None:
+        src_off = np.full(B, int(prefix_len.max()), dtype=np.int32)
+
+    def draw(tag, shape):
+        a = rng_for(seed, name + "." + tag).standard_normal(shape, dtype=np.float32)
+        return act_bits(a, dtype)
+
+    return AttentionCase(draw("q", (B, L, Hq, D)), draw("k_new", (B, L, Hkv, D)),
+                         draw("v_new", (B, L, Hkv, D)), draw("k_cache", (B, Hkv, S_cap, D)),
+                         draw("v_cache", (B, Hkv, S_cap, D)), prefix_len,
+                         np.asarray(src_off, dtype=np.int32), dtype)
+
+
+# The seeded workloads, by what they are. Seed 0 throughout.
 WORKLOADS = {
     "tiny_w4_verify_m8_k512_n1024": dict(M=8, K=512, N=1024, dtype="bf16", x_scale=1.0,
                                           B=1, L=8),
@@ -157,4 +196,10 @@ WORKLOADS = {
                                               x_scale=1.0, B=4, L=16, p=0.7),
     "commit_b4_l16_then_verify_m64": dict(layers=8, B=4, H=8, S_cap=2048, D=128, block=16,
                                           M=64, K=5120, N=17408, dtype="bf16"),
+    # the verify block's attention over the same cache shape (fp16, 8 KV heads x 128,
+    # prefixes ~U(200, 1800)), with 32 query heads (4 per KV head) and rotary
+    # embedding over all 128 dimensions at base 1e6
+    "verify_attention_b4_l16_hq32_hkv8_d128": dict(B=4, L=16, Hq=32, Hkv=8, D=128, S_cap=2048,
+                                                   prefix_lo=200, prefix_hi=1800, dtype="f16",
+                                                   rotary_dim=128, theta=1.0e6),
 }
