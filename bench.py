@@ -67,6 +67,10 @@ def parse_args():
     ap.add_argument("--vocab", action="store_true",
                     help="time the vocabulary projection with the fused arg max instead "
                          "(M=64 rows = B 4 x block 16, K=2560, N=151936)")
+    ap.add_argument("--attn", action="store_true",
+                    help="time the verify block's attention over the per-row cache instead "
+                         "(B=4 x block 16, 32 query / 8 KV heads x 128, fp16, prefixes "
+                         "~U(200, 1800), cache 2048 slots)")
     ap.add_argument("--rows", type=int, default=M, choices=[8, 64],
                     help="rows of the timed verify projection: 8 (the headline block) or 64 "
                          "(the next-block verify GEMM, B=4 x block 16)")
@@ -123,12 +127,20 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# Translation units that hold none of the projection and arg max kernels the
+# profiles cover (they only include headers the digest already covers).
+UNPROFILED_UNITS = ("vq_attn.cu", "vq_selftest.cu")
+
+
 def source_digest() -> str:
-    """sha256 over the CUDA sources: ties a profile's counters to this code."""
+    """sha256 over the CUDA sources the projection and arg max kernels are built
+    from: ties a profile's counters to this code. The attention and wait
+    self-test units are left out, so changing them does not orphan those
+    profiles."""
     csrc = os.path.join(ROOT, "speculative_block_draft_02_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+        if name.endswith((".cu", ".cuh")) and name not in UNPROFILED_UNITS:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -438,6 +450,108 @@ def run_vocab(args):
         dist.destroy_process_group()
 
 
+def attention_bytes(case):
+    """Algorithmic HBM bytes of one verify_attention call: the prefix keys and
+    values it reads, the block's q, k, v, the appended cache slots and the output
+    (the per-chunk partial results stay in L2 and are not counted)."""
+    B, L, Hq, D = case.q.shape
+    Hkv = case.k_new.shape[2]
+    prefix = int(np.asarray(case.prefix_len, dtype=np.int64).sum()) * Hkv * D * 2 * 2
+    block_in = (B * L * Hq * D + 2 * B * L * Hkv * D) * 2
+    return prefix + block_in + 2 * B * L * Hkv * D * 2 + B * L * Hq * D * 2
+
+
+def attention_flops(case):
+    B, L, Hq, D = case.q.shape
+    keys = sum(int(p) * L + L * (L + 1) // 2 for p in case.prefix_len)   # visible (query, key) pairs
+    return 2 * 2 * keys * Hq * D
+
+
+def run_attn(args):
+    """The verify block's attention (B=4 x block 16, 32 / 8 heads x 128, fp16)
+    as the timed step: one JSON line with its time and roofline."""
+    import math
+
+    from speculative_block_draft_02_gb300 import binding as vq
+    from speculative_block_draft_02_gb300 import build, synth
+
+    rank, world, local = dist_setup()
+    build.build()
+    vq.lib()
+    dev = torch.cuda.current_device()
+    K_steps, W = args.steps, max(3, args.warmup)
+    wl = "verify_attention_b4_l16_hq32_hkv8_d128"
+    cfg = synth.WORKLOADS[wl]
+    case = synth.attention_case(0, B=cfg["B"], L=cfg["L"], Hq=cfg["Hq"], Hkv=cfg["Hkv"],
+                                D=cfg["D"], S_cap=cfg["S_cap"], prefix_lo=cfg["prefix_lo"],
+                                prefix_hi=cfg["prefix_hi"], dtype=cfg["dtype"])
+    B, L, Hq, D = case.q.shape
+    Hkv, S_cap = cfg["Hkv"], cfg["S_cap"]
+    t16 = lambda a: torch.from_numpy(a.view(np.int16).copy()).view(torch.float16).cuda()
+    q, kn, vn = t16(case.q), t16(case.k_new), t16(case.v_new)
+    # rotating cache copies (K and V of one layer each) so that every call reads HBM
+    n_cp = n_copies_for(case.k_cache.nbytes + case.v_cache.nbytes)
+    kc0, vc0 = t16(case.k_cache), t16(case.v_cache)
+    caches = [(kc0.clone(), vc0.clone()) for _ in range(n_cp)]
+    del kc0, vc0
+    pl = torch.from_numpy(case.prefix_len).cuda()
+    so = torch.from_numpy(case.src_off).cuda()
+    ws = torch.zeros(vq.verify_attention_workspace_bytes(B, L, Hq, Hkv, D, S_cap),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    scale = 1.0 / math.sqrt(D)
+    calls = [(lambda kc=kc, vc=vc: vq.verify_attention(q, kn, vn, kc, vc, pl, so, ws,
+                                                       cfg["rotary_dim"], cfg["theta"], scale,
+                                                       out=out))
+             for kc, vc in caches]
+    clocks = ClockSampler(dev)
+    total, per_call = time_calls(calls, K_steps, W, world, per_graph=200)
+    clk = clocks.stop()
+    peak, peak_kind = measured_peaks()
+    nbytes = attention_bytes(case)
+    achieved = nbytes / per_call / 1e9
+    line = {
+        "metric": "verify-block attention rows/s and HBM GB/s", "impl": "ours",
+        "value": world * B * L * K_steps / total, "unit": "rows/s", "n_gpus": world,
+        "steps": K_steps, "warmup": W, "ms_per_step": total / K_steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": wl, "B": B, "L": L, "Hq": Hq, "Hkv": Hkv, "D": D,
+                   "S_cap": S_cap, "prefix_len": [int(v) for v in case.prefix_len],
+                   "l2": "inputs > L2: %d rotating cache copies" % n_cp},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": profiled_traffic("verify_attention_f16_b4_l16"),
+                     "algorithmic_bytes": nbytes, "flops": attention_flops(case),
+                     "tflops": attention_flops(case) / per_call / 1e12,
+                     "kernel": "verify_attn_partial_kernel + verify_attn_combine_kernel "
+                               "(time per call, both launches)",
+                     "us_per_launch": per_call * 1e6},
+        "gpu_launches": 2 * K_steps, "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu:
+        import oracle
+
+        oracle.build()
+        reps, t0 = 0, time.perf_counter()
+        while reps < 1 or time.perf_counter() - t0 < 5.0:
+            kco, vco = case.k_cache.copy(), case.v_cache.copy()
+            oracle.verify_attention(case.q, case.k_new, case.v_new, kco, vco, case.prefix_len,
+                                    case.src_off, 1, cfg["rotary_dim"], cfg["theta"], scale)
+            reps += 1
+        t = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": B * L * reps / t, "unit": "rows/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": "%d full calls of the workload, fp64 scalar C, OpenMP "
+                                          "over queries" % reps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
 def path_table(vq, copies, x, W, world):
     """Every other step of the hot path, each at its own workload, timed the
     same way (fewer launches): microseconds per launch and algorithmic GB/s."""
@@ -615,6 +729,8 @@ def main():
         run_reference(args)
     elif args.vocab:
         run_vocab(args)
+    elif args.attn:
+        run_attn(args)
     else:
         run_ours(args)
 

@@ -12,6 +12,9 @@
  *   verify_accept_walk   the per-row accept walk
  *   kv_compact_per_row   the per-row KV commit
  *
+ * verify_attention is the attention of the verify block inside the target's
+ * forward pass, over the same per-row cache the KV commit maintains.
+ *
  * Common rules
  *   - Every tensor pointer is caller-owned DEVICE memory unless a parameter
  *     says otherwise. The library allocates nothing.
@@ -266,6 +269,55 @@ int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Attention of the verify block over the per-row KV cache, one layer.
+ *
+ * Source: mlxcel #2865 "perf(speculative): commit per-row accepts in batched
+ * DFlash", Summary and commit message -- with per-row accept counts the
+ * target rotates the verify block at each row's logical positions and masks,
+ * for every query, the stale gap between the row's valid prefix and the
+ * verify slots that the rectangular cache shares across rows.
+ *
+ * For each batch row b (P = prefix_len[b], S = src_off[b]) and block position
+ * j = 0..L-1, at logical position P + j:
+ *   1. the block's key k_new[b][j][h] is rotated at P + j, rounded to the
+ *      storage type and written to slot S + j of k_cache; v_new[b][j][h] is
+ *      copied to slot S + j of v_cache;
+ *   2. the query q[b][j][hq] is rotated at P + j and rounded to the storage
+ *      type; it reads KV head hq / (Hq / Hkv);
+ *   3. out[b][j][hq] = softmax over the visible slots of scale * (q . k),
+ *      applied to v, where the visible slots are 0..P-1 (the row's valid
+ *      prefix) and S..S+j (the block, causally). Slots P..S-1 (the stale gap)
+ *      and everything after S + j are masked.
+ * Rotation: within the first rotary_dim dimensions, dimension i < rotary_dim/2
+ * pairs with i + rotary_dim/2 and turns by pos * theta^(-2i/rotary_dim)
+ * (y_i = x_i cos - x_{i+h} sin, y_{i+h} = x_{i+h} cos + x_i sin); dimensions
+ * from rotary_dim on are not rotated. The softmax and its sums are fp32.
+ *
+ * q, out        [B][L][Hq][D]; k_new, v_new [B][L][Hkv][D];
+ * k_cache, v_cache  [B][Hkv][S_cap][D], keys stored rotated. All 16-bit of
+ *               `dtype` (VQ_BF16 or VQ_F16); q, k_new, v_new and the caches
+ *               16-byte aligned, out 2-byte aligned; no tensor overlaps
+ *               another.
+ * prefix_len, src_off  int32 [B] on the device.
+ * status        optional int32 on the device: a row with P < 0, S < P or
+ *               S + L > S_cap is left untouched in the caches, gets zero
+ *               output, and bit 0 is OR-ed into *status (never cleared).
+ * workspace     verify_attention_workspace_bytes(...) bytes, 16-byte aligned;
+ *               no initial contents needed.
+ * Sizes         B >= 1, 1 <= L <= 64, Hq a multiple of Hkv, D 64 or 128
+ *               (VQ_EUNSUPPORTED otherwise), L <= S_cap <= 2^24, rotary_dim
+ *               even in 0..D, theta > 0 when rotary_dim > 0.
+ * Two kernels: one per (chunk of 128 keys, KV head, group of 64 query rows,
+ * batch row), then one that merges the chunks.
+ */
+size_t verify_attention_workspace_bytes(int B, int L, int Hq, int Hkv, int D, int S_cap);
+int verify_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                     void* v_cache, const int32_t* prefix_len, const int32_t* src_off,
+                     void* out, int B, int L, int Hq, int Hkv, int D, int S_cap, int rotary_dim,
+                     double theta, double scale, int dtype, int32_t* status, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
  * The launch plan a projection or arg max call would use, computed on the
  * host for a device with `sm_count` SMs (no device is touched): which kernel,
  * how deep its shared-memory ring is, how K is split, the grid, and the
@@ -300,6 +352,26 @@ const char* vq_strerror(int code);
  * Synchronizes `stream`. If clear != 0 the word is reset to 0 afterwards.
  */
 int vq_device_error(int32_t* out, int clear, void* stream);
+
+/*
+ * Self-test of the bounded waits the pipelined kernels rely on: one block
+ * waits, with the kernels' own wait helpers, on an mbarrier that completes and
+ * on one that nothing ever arrives at. The stuck waits give up after the
+ * kernels' wait limit (2^31 SM cycles, about a second each; the call runs for
+ * about two seconds) and flag their status word instead of hanging. The pages
+ * have no counterpart: this checks that a stuck pipeline in this library ends
+ * with an error status.
+ *
+ * status  int32[2] on the device, zero before the call: bit 0 of status[0] is
+ *         set by the aborting waits, bit 0 of status[1] by the teardown wait.
+ * report  int64[8] on the device: [0] completed-barrier wait succeeded (1),
+ *         [1] its SM cycles, [2] stuck wait succeeded (0), [3] its cycles,
+ *         [4] the block's abort flag afterwards (1), [5] a second warp's wait
+ *         on the stuck barrier succeeded (0), [6] its cycles (short: it sees
+ *         the abort flag), [7] cycles of the teardown wait on it.
+ * The library's own status word (vq_device_error) is not touched.
+ */
+int vq_wait_selftest(int32_t* status, int64_t* report, void* stream);
 
 #ifdef __cplusplus
 }

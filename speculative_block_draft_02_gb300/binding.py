@@ -21,7 +21,7 @@ VQ_BF16, VQ_F16, VQ_F32 = 0, 1, 2
 _ACT = {torch.bfloat16: VQ_BF16, torch.float16: VQ_F16, torch.float32: VQ_F32}
 
 # Every symbol include/vq.h declares, with its ctypes signature.
-_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_P, _I, _S, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_double
 SIGNATURES = {
     "vq_linear_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "vq_linear": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _P, _S, _P]),
@@ -35,9 +35,13 @@ SIGNATURES = {
     "verify_round_workspace_bytes": (_S, [_I, _I]),
     "verify_round": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                           _I, _P, _P, _P, _P, _P, _S, _P]),
+    "verify_attention_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
+    "verify_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _D, _D,
+                              _I, _P, _P, _S, _P]),
     "vq_plan": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "vq_strerror": (ctypes.c_char_p, [_I]),
     "vq_device_error": (_I, [_P, _I, _P]),
+    "vq_wait_selftest": (_I, [_P, _P, _P]),
 }
 
 _lib = None
@@ -219,6 +223,47 @@ class _Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("kernel", "rows_padded", "stages", "prefetch",
                                                "k_splits", "units", "grid", "launches")] + \
                [("smem_bytes", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+
+
+def verify_attention_workspace_bytes(B: int, L: int, Hq: int, Hkv: int, D: int,
+                                     S_cap: int) -> int:
+    return int(lib().verify_attention_workspace_bytes(B, L, Hq, Hkv, D, S_cap))
+
+
+def verify_attention(q, k_new, v_new, k_cache, v_cache, prefix_len, src_off, workspace,
+                     rotary_dim: int, theta: float, scale: float, out=None, status=None,
+                     stream=None):
+    """Attention of the verify block q [B][L][Hq][D] over the per-row caches
+    [B][Hkv][S_cap][D] (updated in place with the block's rotated keys and its
+    values at slots src_off + j); returns out [B][L][Hq][D]."""
+    B, L, Hq, D = q.shape
+    Hkv, S_cap = k_cache.shape[1], k_cache.shape[2]
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise VQError("verify_attention takes bf16 or f16 tensors")
+    for t in (k_new, v_new, k_cache, v_cache):
+        if t.dtype != q.dtype:
+            raise VQError("verify_attention: every tensor must have q's dtype")
+    if tuple(k_new.shape) != (B, L, Hkv, D) or tuple(v_new.shape) != (B, L, Hkv, D) or \
+            tuple(v_cache.shape) != tuple(k_cache.shape) or k_cache.shape[0] != B or \
+            k_cache.shape[3] != D:
+        raise VQError("verify_attention: inconsistent shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib().verify_attention(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(prefix_len), _ptr(src_off), _ptr(out), B, L, Hq, Hkv, D,
+                                S_cap, rotary_dim, float(theta), float(scale), _ACT[q.dtype],
+                                _ptr(status), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(),
+                                _stream(stream))
+    _check(rc, "verify_attention")
+    return out
+
+
+def vq_wait_selftest(status, report, stream=None):
+    """Runs the bounded-wait self-test (about two seconds) into status int32[2]
+    and report int64[8] on the device."""
+    _check(lib().vq_wait_selftest(_ptr(status), _ptr(report), _stream(stream)),
+           "vq_wait_selftest")
 
 
 def vq_plan(M: int, K: int, N: int, act=torch.bfloat16, argmax: bool = False,

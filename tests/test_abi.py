@@ -113,3 +113,47 @@ def test_host_validation_rejects_before_any_launch(vqlib):
     bad = (ctypes.c_void_p * 2)(0x1000, 0x2008)
     assert vqlib.kv_compact_per_row(ctypes.cast(bad, P), 2, 4, 8, 2048, 128, 2, fake, fake, fake,
                                     16, fake, None, None) == -2
+
+
+def test_verify_attention_workspace_and_host_validation(vqlib):
+    P = ctypes.c_void_p
+    # rows of partial results: B * Hkv * ceil(L*G/64) * ceil(S_cap/128) * 64, each
+    # D floats of output plus (max, sum)
+    rows = 4 * 8 * 1 * 16 * 64
+    assert vqlib.verify_attention_workspace_bytes(4, 16, 32, 8, 128, 2048) == rows * (128 * 4 + 8)
+    rows = 2 * 2 * 2 * 1 * 64                      # L*G = 80 rows -> two groups of 64
+    assert vqlib.verify_attention_workspace_bytes(2, 10, 16, 2, 64, 100) == rows * (64 * 4 + 8)
+    assert vqlib.verify_attention_workspace_bytes(2, 10, 15, 2, 64, 100) == 0
+
+    fake = P(0x1000)
+    ws_need = vqlib.verify_attention_workspace_bytes(4, 16, 32, 8, 128, 2048)
+
+    def call(q=fake, out=fake, B=4, L=16, Hq=32, Hkv=8, D=128, S_cap=2048, rd=128, theta=1e6,
+             scale=0.088, dtype=1, ws=fake, ws_bytes=ws_need):
+        # every call below fails validation before any CUDA work
+        return vqlib.verify_attention(q, fake, fake, fake, fake, fake, fake, out, B, L, Hq, Hkv, D,
+                                      S_cap, rd, theta, scale, dtype, None, ws, ws_bytes, None)
+
+    assert call(B=0) == -1
+    assert call(Hq=30) == -1                       # not a multiple of Hkv
+    assert call(S_cap=8) == -1                     # shorter than the block
+    assert call(rd=7) == -1 and call(rd=130) == -1
+    assert call(theta=0.0) == -1 and call(theta=float("nan")) == -1
+    assert call(scale=float("inf")) == -1
+    assert call(dtype=2) == -1                     # fp32 tensors are not taken
+    assert call(q=None) == -1
+    assert call(D=96, rd=96) == -4
+    assert call(L=65, S_cap=4096) == -4
+    assert call(q=P(0x1008)) == -2                 # 16-byte alignment
+    assert call(out=P(0x1001)) == -2
+    assert call(ws=None) == -5
+    assert call(ws_bytes=ws_need - 1) == -5
+    assert call(ws=P(0x1008)) == -5
+
+
+def test_wait_selftest_host_validation(vqlib):
+    P = ctypes.c_void_p
+    assert vqlib.vq_wait_selftest(None, P(0x1000), None) == -1
+    assert vqlib.vq_wait_selftest(P(0x1000), None, None) == -1
+    assert vqlib.vq_wait_selftest(P(0x1002), P(0x1000), None) == -2
+    assert vqlib.vq_wait_selftest(P(0x1000), P(0x1004), None) == -2
