@@ -19,8 +19,11 @@
 //       output and its (max, sum) per row to the workspace.
 //   verify_attn_combine_kernel  merges the chunks of every query row and writes
 //       the 16-bit output.
-// The data movement is plain 16-byte loads: the chunks are small (at most 64 KB
-// of K and V per block) and every block reads its own slice once.
+// The chunks are small (at most 64 KB of K and V per block) and every block
+// reads its own slice once, so the staging is 16-byte pieces, all requested
+// before any is waited for: cp.async for the query rows and keys, register
+// loads for the values (transposed into shared memory). The merge is launched
+// with programmatic stream serialization and waits for the partial kernel.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -86,6 +89,18 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
   lo = (uint32_t)f2h<kF16>(a - h2f<kF16>(ha)) | ((uint32_t)f2h<kF16>(b - h2f<kF16>(hb)) << 16);
 }
 
+// 16 bytes global -> shared without a register round trip; zeros when !valid
+// (nothing is read then).
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_u32(const uint16_t* p) {
   return *reinterpret_cast<const uint32_t*>(p);
 }
@@ -125,10 +140,53 @@ __global__ void __launch_bounds__(kAttnThreads)
   if (c0 >= T) return;
   const int tid = threadIdx.x;
   const int rh = p.rot_half;
+  grid_launch_dependents();
 
-  // (cos, sin) of every block position's angles. The angle pos * f is formed as
-  // a + err with a = fl(pos * hi) and err the rest of pos * (hi + lo), then turned
-  // to first order: sin(a + err) ~ sin a + err cos a (|err| < 1e-3 rad).
+  // Every load of the stage is issued before any of them is waited for: the
+  // query rows and the keys go global -> shared asynchronously, the values
+  // (transposed on the way) through registers.
+  // Query rows of this group: row r = j * G + (hq - hk * G).
+  for (int i = tid; i < kAttnRows * DC; i += kAttnThreads) {
+    const int r = i / DC, dc = i - r * DC;
+    const int rr = rg * kAttnRows + r;
+    const uint16_t* src = p.q;
+    if (rr < p.R) {
+      const int j = rr / p.G, hq = hk * p.G + (rr - j * p.G);
+      src = p.q + (((size_t)b * p.L + j) * p.Hq + hq) * D + dc * 8;
+    }
+    cp_async_16(Qs + r * QS + dc * 8, src, rr < p.R);
+  }
+  // Keys: prefix slots from the cache, the block's keys (rotated below), zeros past T.
+  for (int i = tid; i < kChunk * DC; i += kAttnThreads) {
+    const int tl = i / DC, dc = i - tl * DC;
+    const int t = c0 + tl;
+    const uint16_t* src = p.k_cache;
+    if (t < P) {
+      src = p.k_cache + (((size_t)b * p.Hkv + hk) * p.S_cap + t) * D + dc * 8;
+    } else if (t < T) {
+      src = p.k_new + (((size_t)b * p.L + (t - P)) * p.Hkv + hk) * D + dc * 8;
+    }
+    cp_async_16(Ks + tl * QS + dc * 8, src, t < T);
+  }
+  // Values: thread tid owns key c0 + tid.
+  uint4 vv[DC];
+  {
+    const int t = c0 + tid;
+    const uint16_t* src = nullptr;
+    if (t < P) {
+      src = p.v_cache + (((size_t)b * p.Hkv + hk) * p.S_cap + t) * D;
+    } else if (t < T) {
+      src = p.v_new + (((size_t)b * p.L + (t - P)) * p.Hkv + hk) * D;
+    }
+#pragma unroll
+    for (int dc = 0; dc < DC; ++dc)
+      vv[dc] = src ? __ldg(reinterpret_cast<const uint4*>(src) + dc) : make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  // (cos, sin) of every block position's angles, while the loads are in flight.
+  // The angle pos * f is formed as a + err with a = fl(pos * hi) and err the rest
+  // of pos * (hi + lo), then turned to first order: sin(a + err) ~ sin a + err cos a
+  // (|err| < 1e-3 rad).
   for (int i = tid; i < p.L * rh; i += kAttnThreads) {
     const int j = i / rh, e = i - j * rh;
     const float pos = (float)(P + j);
@@ -140,53 +198,16 @@ __global__ void __launch_bounds__(kAttnThreads)
     cs[i] = make_float2(c - err * s, s + err * c);
   }
 
-  // Query rows of this group: row r = j * G + (hq - hk * G).
-  for (int i = tid; i < kAttnRows * DC; i += kAttnThreads) {
-    const int r = i / DC, dc = i - r * DC;
-    const int rr = rg * kAttnRows + r;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (rr < p.R) {
-      const int j = rr / p.G, hq = hk * p.G + (rr - j * p.G);
-      v = __ldg(reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.L + j) * p.Hq + hq) * D) +
-                dc);
-    }
-    *reinterpret_cast<uint4*>(Qs + r * QS + dc * 8) = v;
-  }
-  // Keys: prefix slots from the cache, the block's keys (rotated below), zeros past T.
-  for (int i = tid; i < kChunk * DC; i += kAttnThreads) {
-    const int tl = i / DC, dc = i - tl * DC;
-    const int t = c0 + tl;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (t < P) {
-      v = __ldg(reinterpret_cast<const uint4*>(
-                    p.k_cache + (((size_t)b * p.Hkv + hk) * p.S_cap + t) * D) + dc);
-    } else if (t < T) {
-      v = __ldg(reinterpret_cast<const uint4*>(
-                    p.k_new + (((size_t)b * p.L + (t - P)) * p.Hkv + hk) * D) + dc);
-    }
-    *reinterpret_cast<uint4*>(Ks + tl * QS + dc * 8) = v;
-  }
-  // Values, transposed: thread tid owns key c0 + tid.
-  {
-    const int t = c0 + tid;
-    const uint16_t* src = nullptr;
-    if (t < P) {
-      src = p.v_cache + (((size_t)b * p.Hkv + hk) * p.S_cap + t) * D;
-    } else if (t < T) {
-      src = p.v_new + (((size_t)b * p.L + (t - P)) * p.Hkv + hk) * D;
-    }
-#pragma unroll 4
-    for (int dc = 0; dc < DC; ++dc) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (src) v = __ldg(reinterpret_cast<const uint4*>(src) + dc);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        Vt[(dc * 8 + 2 * e) * VS + tid] = (uint16_t)(w[e] & 0xFFFFu);
-        Vt[(dc * 8 + 2 * e + 1) * VS + tid] = (uint16_t)(w[e] >> 16);
-      }
+  for (int dc = 0; dc < DC; ++dc) {
+    const uint32_t w[4] = {vv[dc].x, vv[dc].y, vv[dc].z, vv[dc].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      Vt[(dc * 8 + 2 * e) * VS + tid] = (uint16_t)(w[e] & 0xFFFFu);
+      Vt[(dc * 8 + 2 * e + 1) * VS + tid] = (uint16_t)(w[e] >> 16);
     }
   }
+  cp_async_wait_all();
   __syncthreads();
 
   // Rotate the queries and the block's keys at their logical positions P + j.
@@ -336,6 +357,7 @@ __global__ void __launch_bounds__(D) verify_attn_combine_kernel(const __grid_con
   const int jh = blockIdx.x, b = blockIdx.y;
   const int j = jh / p.Hq, hq = jh - j * p.Hq;
   const int d = threadIdx.x;
+  grid_wait_prerequisites();   // launched early (programmatic serialization)
   uint16_t* dst = p.out + (((size_t)b * p.L + j) * p.Hq + hq) * D;
   const int P = p.prefix_len[b], S = p.src_off[b];
   if (!row_in_range(P, S, p.L, p.S_cap)) {
@@ -413,8 +435,20 @@ int attn_launch(const AttnParams& p, int B, cudaStream_t stream) {
     return VQ_ECUDA;
   partial<<<dim3(p.NC, p.Hkv * p.RG, B), kAttnThreads, smem, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return VQ_ECUDA;
-  verify_attn_combine_kernel<kF16, D><<<dim3(p.L * p.Hq, B), D, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return VQ_ECUDA;
+  // the merge may be scheduled while the partial kernel runs; it waits for it
+  // (griddepcontrol.wait) before reading anything
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.L * p.Hq, B);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, verify_attn_combine_kernel<kF16, D>, p) != cudaSuccess)
+    return VQ_ECUDA;
   return VQ_OK;
 }
 
