@@ -132,27 +132,35 @@ def measured_peaks():
 UNPROFILED_UNITS = ("vq_attn.cu", "vq_selftest.cu")
 
 
-def source_digest() -> str:
-    """sha256 over the CUDA sources the projection and arg max kernels are built
-    from: ties a profile's counters to this code. The attention and wait
-    self-test units are left out, so changing them does not orphan those
-    profiles."""
+# The sources the attention kernels are built from.
+ATTENTION_UNITS = ("vq_attn.cu", "vq_common.cuh")
+
+
+def source_digest(units=None) -> str:
+    """sha256 over CUDA sources: ties a profile's counters to this code. By
+    default the sources the projection and arg max kernels are built from (the
+    attention and wait self-test units are left out, so changing them does not
+    orphan those profiles); `units` names another set."""
     csrc = os.path.join(ROOT, "speculative_block_draft_02_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")) and name not in UNPROFILED_UNITS:
+        if units is not None:
+            take = name in units
+        else:
+            take = name.endswith((".cu", ".cuh")) and name not in UNPROFILED_UNITS
+        if take:
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_tag: str):
+def profiled_traffic(kernel_tag: str, units=None):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current sources (else None)."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    digest = source_digest()
+    digest = source_digest(units)
     for name in sorted(os.listdir(pdir)):
         if kernel_tag not in name:
             continue
@@ -521,7 +529,8 @@ def run_attn(args):
                    "l2": "inputs > L2: %d rotating cache copies" % n_cp},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": profiled_traffic("verify_attention_f16_b4_l16"),
+                     "traffic": profiled_traffic("verify_attention_f16_b4_l16",
+                                                 ATTENTION_UNITS),
                      "algorithmic_bytes": nbytes, "flops": attention_flops(case),
                      "tflops": attention_flops(case) / per_call / 1e12,
                      "kernel": "verify_attn_partial_kernel + verify_attn_combine_kernel "
