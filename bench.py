@@ -136,11 +136,37 @@ UNPROFILED_UNITS = ("vq_attn.cu", "vq_selftest.cu")
 ATTENTION_UNITS = ("vq_attn.cu", "vq_common.cuh")
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed: what
+    the compiler sees, so that comment or layout edits do not orphan a profile."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif c == "/" and text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_digest(units=None) -> str:
-    """sha256 over CUDA sources: ties a profile's counters to this code. By
-    default the sources the projection and arg max kernels are built from (the
-    attention and wait self-test units are left out, so changing them does not
-    orphan those profiles); `units` names another set."""
+    """sha256 over the code (comments stripped) of CUDA sources: ties a
+    profile's counters to the code they were taken on. By default the sources
+    the projection and arg max kernels are built from (the attention and wait
+    self-test units are left out, so changing them does not orphan those
+    profiles); `units` names another set."""
     csrc = os.path.join(ROOT, "speculative_block_draft_02_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
@@ -149,8 +175,8 @@ def source_digest(units=None) -> str:
         else:
             take = name.endswith((".cu", ".cuh")) and name not in UNPROFILED_UNITS
         if take:
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
