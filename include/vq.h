@@ -201,9 +201,10 @@ int verify_accept_walk(const int32_t* draft, const int32_t* target, int B, int L
 /*
  * Per-row KV commit (compaction to a contiguous valid prefix).
  *
- * Source: mlxcel #2865, Summary -- the target compacts its attention KV back
- * to per-row contiguous valid prefixes so that every row keeps its own accept
- * count in a rectangular cache.
+ * Source: mlxcel #2865, Summary -- after each round the target's attention
+ * cache is packed again so that every row's valid tokens form one unbroken
+ * run from slot 0, which lets each row keep its own accept count in a
+ * rectangular cache.
  *
  * For each of the n_tensors tensors (e.g. K and V of every layer), each row b
  * and head h: slots src_off[b] .. src_off[b]+keep[b]-1, as they were before
@@ -272,10 +273,11 @@ int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
  * Attention of the verify block over the per-row KV cache, one layer.
  *
  * Source: mlxcel #2865 "perf(speculative): commit per-row accepts in batched
- * DFlash", Summary and commit message -- with per-row accept counts the
- * target rotates the verify block at each row's logical positions and masks,
- * for every query, the stale gap between the row's valid prefix and the
- * verify slots that the rectangular cache shares across rows.
+ * DFlash", Summary and commit message -- with per-row accept counts, the
+ * rotary embedding and the attention of the verify block use every row's own
+ * logical positions, and each query is kept from seeing the stale gap between
+ * its row's valid prefix and the verify slots the rectangular cache shares
+ * across rows.
  *
  * For each batch row b (P = prefix_len[b], S = src_off[b]) and block position
  * j = 0..L-1, at logical position P + j:

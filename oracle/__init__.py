@@ -17,8 +17,8 @@ and which passage of the pages it follows, is stated in the C file:
   (mlxcel #2865, Summary).
 * ``kv_compact``  -- per-row KV commit to a contiguous valid prefix
   (mlxcel #2865, Summary).
-* ``verify_attention`` -- the verify block's attention at each row's logical
-  positions with the stale gap masked (mlxcel #2865, Summary and commit
+* ``verify_attention`` -- the verify block's attention, rotated at every row's
+  own logical positions, no query seeing the stale gap (mlxcel #2865, Summary and commit
   message), with ``round_bits`` its rounding to the 16-bit storage formats.
 """
 from __future__ import annotations

@@ -19,7 +19,7 @@
  *    y[m][n] = sum over k = 0..K-1, in ascending k, of x[m][k] * w(n,k).
  *    All M rows of the block use the same weights (ds4 #778 "dspark: fold
  *    first-token forward into verify ...", commit 1 message: the row tiles
- *    that stop reading every dense weight twice).
+ *    read each dense weight once instead of twice).
  *
  *  - The greedy target token of a verify row is the arg max of its logits
  *    (ds4 #778, commit 1 message: greedy, temperature 0). The decision is

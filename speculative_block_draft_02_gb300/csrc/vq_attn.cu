@@ -2,9 +2,9 @@
 //
 // mlxcel #2865 "perf(speculative): commit per-row accepts in batched DFlash",
 // Summary and commit message: once every batch row keeps its own accept count,
-// the target rotates the verify block at each row's logical positions and
-// masks, for every query, the stale gap between the row's valid prefix and the
-// verify slots the rectangular cache shares across rows.
+// the rotary embedding and the attention of the verify block use every row's
+// own logical positions, and no query sees the stale gap between its row's
+// valid prefix and the verify slots the rectangular cache shares across rows.
 //
 // Two kernels per call:
 //   verify_attn_partial_kernel  one block per (key chunk of 128, KV head, group
