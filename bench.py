@@ -8,6 +8,10 @@ line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+Other timed steps, each on its own JSON line: --rows 64 (the next-block verify
+projection, B=4 x block 16), --vocab (the vocabulary projection with the fused
+arg max), --attn (the verify block's attention over the per-row cache).
+
 Timing: W untimed steps, then exactly K steps replayed from CUDA graphs on one
 stream, bracketed by a barrier and torch.cuda.synchronize(), CUDA events on
 that stream; the max over ranks is reported. The weights rotate over enough
