@@ -1,10 +1,11 @@
 """GPU parity: the CUDA library, called through its C ABI, against the oracle.
 
 Projections must meet the tolerance in parity.py; arg max indices, accept
-lengths and compacted KV must match bit for bit. Small shapes are checked in
-full (several 128-row units, several 512-wide stages and ragged tails);
-the full-size workloads are checked on sampled output columns (all M rows)
-or, for the arg max, in full.
+lengths and compacted KV must match bit for bit. Every projection, the
+full-size workloads included, is compared with the oracle element by element
+over its whole output (the oracle takes well under a second for the largest
+of them); small shapes span several 128-row units, several 512-wide stages and
+ragged tails.
 """
 import numpy as np
 import pytest
@@ -91,9 +92,7 @@ def test_linear_ragged_shapes(M, K, N, dtype):
 def test_linear_wide_n_x_table(M, K, N, dtype):
     w = synth.w4_weights(M + K, N, K)
     x = synth.activations(M + K, M, K, dtype)
-    y = run_linear(x, w, dtype)
-    cols = _sample_cols(N, 3, 300)
-    assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
+    assert_proj_close(run_linear(x, w, dtype), oracle_linear(x, w, dtype), dtype)
 
 
 # 16-bit x with M > 16 and an N wide enough that K is not split: the
@@ -108,9 +107,7 @@ def test_linear_tensor_core_path(M, K, N, dtype):
     seed = 7 * M + K + N
     w = synth.w4_weights(seed, N, K)
     x = synth.activations(seed, M, K, dtype)
-    y = run_linear(x, w, dtype)
-    cols = _sample_cols(N, 5, 200)
-    assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
+    assert_proj_close(run_linear(x, w, dtype), oracle_linear(x, w, dtype), dtype)
 
 
 # long K on the tcgen05 kernel: the group row sums are taken per stage from
@@ -120,9 +117,7 @@ def test_linear_tensor_core_long_k(M, K, N, dtype):
     seed = 11 * M + K
     w = synth.w4_weights(seed, N, K)
     x = synth.activations(seed, M, K, dtype)
-    y = run_linear(x, w, dtype)
-    cols = _sample_cols(N, 9, 150)
-    assert_proj_close(y[:, cols], oracle_linear(x, w, dtype, cols), dtype)
+    assert_proj_close(run_linear(x, w, dtype), oracle_linear(x, w, dtype), dtype)
 
 
 def test_vocab_argmax_tensor_core_long_k():
@@ -154,10 +149,9 @@ def test_linear_x_table_handles_large_and_tiny_rows():
     base[2, ::7] = 0.0
     x = synth.to_bf16_bits(base)
     y = run_linear(x, w, "bf16")
-    cols = _sample_cols(N, 4, 200)
-    r = oracle_linear(x, w, "bf16", cols)
+    r = oracle_linear(x, w, "bf16")
     for m in range(M):
-        assert_proj_close(y[m:m + 1, cols], r[m:m + 1], "bf16")
+        assert_proj_close(y[m:m + 1], r[m:m + 1], "bf16")
 
 
 @pytest.mark.parametrize("M,K,N", [(8, 5120, 1024), (4, 4096, 256), (16, 2560, 640)])
@@ -172,20 +166,13 @@ def test_linear_split_k_is_exact_and_repeatable(M, K, N):
     assert_proj_close(y1, oracle_linear(x, w, "bf16"), "bf16")
 
 
-def _sample_cols(N, seed, n_random=200):
-    r = np.random.default_rng(seed)
-    cols = np.concatenate([np.arange(0, 128), np.arange(N - 128, N),
-                           r.choice(N, size=n_random, replace=False)])
-    return np.unique(cols).astype(np.int32)
-
-
-def test_linear_paper_shape_sampled():
-    # M=8, K=5120, N=17408, bf16 ~N(0,1): the headline verify projection
-    w = synth.w4_weights(0, 17408, 5120)
+@pytest.mark.parametrize("N", [17408, 1024])
+def test_linear_paper_shape_full(N):
+    # M=8, K=5120, N=17408 and N=1024, bf16 ~N(0,1): the headline verify
+    # projection and its narrow-output case, every output element
+    w = synth.w4_weights(0, N, 5120)
     x = synth.activations(0, 8, 5120, "bf16")
-    y = run_linear(x, w, "bf16")
-    cols = _sample_cols(17408, 1)
-    assert_proj_close(y[:, cols], oracle_linear(x, w, "bf16", cols), "bf16")
+    assert_proj_close(run_linear(x, w, "bf16"), oracle_linear(x, w, "bf16"), "bf16")
 
 
 @pytest.fixture(scope="module")
@@ -198,8 +185,7 @@ def sweep_weights():
 def test_linear_block_size_and_dtype_sweep(sweep_weights, M, dtype):
     x = synth.activations(0, M, 5120, dtype, scale=0.5)
     y = run_linear(x, sweep_weights, dtype)
-    cols = _sample_cols(17408, M, 100)
-    assert_proj_close(y[:, cols], oracle_linear(x, sweep_weights, dtype, cols), dtype)
+    assert_proj_close(y, oracle_linear(x, sweep_weights, dtype), dtype)
 
 
 def test_rows_are_independent_and_permute():
@@ -359,7 +345,10 @@ def test_vocab_argmax_full_workload_and_accept():
     x = synth.activations(0, cfg["M"], cfg["K"], "bf16")
     idx, mx, _ = run_vocab(x, w)
     logits = oracle_linear(x, w, "bf16")
-    check_argmax(idx, mx, logits)
+    # no row of this workload has its top two logits within the near-tie
+    # margin (the smallest relative top-1/top-2 gap is 8.3e-4), so every index
+    # must match bit for bit
+    assert check_argmax(idx, mx, logits) == 0
     r_idx, _, _ = oracle.argmax(logits)
     target = r_idx.reshape(cfg["B"], cfg["L"])
     draft = synth.drafts_from_target(0, target, cfg["N"], cfg["p"])
@@ -445,9 +434,7 @@ def test_commit_then_next_block_verify():
     assert np.array_equal(new_len, case.prefix_len + case.keep)
     w = synth.w4_weights(0, cfg["N"], cfg["K"])
     x = synth.activations(0, cfg["M"], cfg["K"], "bf16", name="x_next")
-    y = run_linear(x, w, "bf16")
-    cols = _sample_cols(cfg["N"], 7, 60)
-    assert_proj_close(y[:, cols], oracle_linear(x, w, "bf16", cols), "bf16")
+    assert_proj_close(run_linear(x, w, "bf16"), oracle_linear(x, w, "bf16"), "bf16")
 
 
 # ------------------------------------------------------------ one verify round
