@@ -132,8 +132,9 @@ def measured_peaks():
 
 
 # Translation units that hold none of the projection and arg max kernels the
-# profiles cover (they only include headers the digest already covers).
-UNPROFILED_UNITS = ("vq_attn.cu", "vq_selftest.cu")
+# profiles cover (they only include headers the digest already covers): the
+# attention, the wait self-test, and the accept walk / KV commit / round glue.
+UNPROFILED_UNITS = ("vq_attn.cu", "vq_selftest.cu", "vq_small.cu")
 
 
 # The sources the attention kernels are built from.
@@ -227,6 +228,18 @@ class ClockSampler:
         except (OSError, ValueError):
             self.proc = None
 
+    def wait_started(self, timeout_s=5.0):
+        """Blocks until nvidia-smi has written its first sample (it takes a
+        while to start), so that the load that follows is sampled."""
+        if self.proc is None:
+            return
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < timeout_s:
+            self.out.flush()
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.01)
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -286,13 +299,10 @@ def dev_act(seed, M_, K_, dtype="bf16", scale=1.0, name="x"):
 
 
 def launches_per_call(vq, M_, K_, N_):
-    # 16-bit x: M <= 8 prepares the x slices, M > 16 (no K split) sums the x
-    # groups in a small kernel before the projection; with a K split there is
-    # no such kernel
-    if M_ <= 8:
-        return 2
-    nb = vq.vq_linear_workspace_bytes(M_, K_, N_, torch.bfloat16)
-    return 2 if M_ > 16 and nb == (K_ // 64) * 64 * 4 else 1
+    # the planner's count: one kernel, plus the group row sums before the
+    # tcgen05 projection where those fit a table
+    return vq.vq_plan(M_, K_, N_, torch.bfloat16, False,
+                      torch.cuda.get_device_properties(0).multi_processor_count)["launches"]
 
 
 def workspace_for(vq, M_, K_, N_, dt):
@@ -312,7 +322,25 @@ def graph_of(calls):
     return g
 
 
-def time_calls(calls, steps, warmup, world=1, per_graph=220):
+# A spin kernel of this many SM cycles (about 100 us) runs ahead of the start
+# event, so that the host has submitted the timed graphs before the GPU
+# reaches the event: the timed region then holds the steps' device time, not
+# the host's submission latency.
+SPIN_CYCLES = 200_000
+# With a clock sampler, the same graphs run untimed for this long before and
+# after the timed region, so that the samples show the clocks under this load
+# (a timed region of a few hundred microseconds is shorter than one sample).
+LOAD_S = 0.4
+
+
+def replay_for(g, seconds):
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        g.replay()
+        torch.cuda.synchronize()
+
+
+def time_calls(calls, steps, warmup, world=1, per_graph=220, clocks=None):
     """Run `steps` calls (cycling through `calls`) from CUDA graphs; returns
     (total seconds over ranks, per-launch seconds)."""
     for i in range(max(warmup, len(calls))):
@@ -324,10 +352,14 @@ def time_calls(calls, steps, warmup, world=1, per_graph=220):
     tail = graph_of([calls[i % len(calls)] for i in range(tail_n)]) if tail_n else None
     body.replay()
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.wait_started()
+        replay_for(body, LOAD_S)
     stream = torch.cuda.current_stream()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda._sleep(SPIN_CYCLES)
     ev[0].record(stream)
     for _ in range(reps):
         body.replay()
@@ -336,8 +368,28 @@ def time_calls(calls, steps, warmup, world=1, per_graph=220):
     ev[1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
+    if clocks is not None:
+        replay_for(body, LOAD_S)
     t = ev[0].elapsed_time(ev[1]) / 1e3
     return max_over_ranks(t, world), t / steps
+
+
+def isolated_launch_stats(calls, n=100):
+    """Median and mean device time of single launches, each bracketed by its
+    own events with a spin kernel ahead of it (no overlap with a neighbouring
+    call): the per-launch distribution beside the back-to-back mean."""
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for i, (a, b) in enumerate(evs):
+        torch.cuda._sleep(SPIN_CYCLES // 10)
+        a.record(stream)
+        calls[i % len(calls)]()
+        b.record(stream)
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    return {"median_us": statistics.median(us), "mean_us": statistics.fmean(us), "n": n,
+            "method": "one launch between two events, a spin kernel ahead of each"}
 
 
 def run_ours(args):
@@ -362,8 +414,9 @@ def run_ours(args):
     calls = [(lambda c=c: vq.vq_linear(x, *c, y=y, workspace=ws)) for c in copies]
 
     clocks = ClockSampler(dev)
-    total, per_launch = time_calls(calls, K_steps, W, world)
+    total, per_launch = time_calls(calls, K_steps, W, world, clocks=clocks)
     clk = clocks.stop()
+    isolated = isolated_launch_stats(calls)
 
     rows_per_s = world * Mr * K_steps / total
     peak, peak_kind = measured_peaks()
@@ -414,8 +467,8 @@ def run_ours(args):
                        parallelism="replicas" if world > 1 else "single",
                        l2="inputs > L2: %d rotating weight copies (%.0f MB)"
                           % (n_cp, n_cp * b_main / 1e6),
-                       timing="CUDA graphs of %d launches, events on the launch stream"
-                              % min(K_steps, 220)),
+                       timing="CUDA graphs of %d launches, events on the launch stream, "
+                              "a spin kernel ahead of the start event" % min(K_steps, 220)),
         "hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
@@ -423,9 +476,11 @@ def run_ours(args):
                      "kernel": ("vq_gemm_kernel<bf16, MT=1, prepared x slices>" if Mr <= 8 else
                                 "vq_tc_kernel<bf16, MP=64> (tcgen05)"),
                      "us_per_launch": per_launch * 1e6,
-                     "launch_note": "per call: a small x-preparation kernel, then the "
-                                    "projection, chained by programmatic dependent launch; "
-                                    "time per call over the timed region"},
+                     "isolated_launch": isolated,
+                     "launch_note": "mean time per call over the timed region (calls back to "
+                                    "back, each overlapping the tail of the one before through "
+                                    "programmatic dependent launch); isolated_launch: single "
+                                    "calls with nothing to overlap"},
         "e2e": e2e, "gpu_launches": K_steps * launches_per_call(vq, Mr, K, N), "clocks": clk,
     }
 
@@ -461,7 +516,7 @@ def run_vocab(args):
     am = torch.empty(Mv, dtype=torch.int32, device="cuda")
     calls = [(lambda c=c: vq.vq_vocab_argmax(xv, *c, wsv, argmax=am)) for c in cv]
     clocks = ClockSampler(dev)
-    total, per_launch = time_calls(calls, K_steps, W, world, per_graph=100)
+    total, per_launch = time_calls(calls, K_steps, W, world, per_graph=100, clocks=clocks)
     clk = clocks.stop()
     peak, peak_kind = measured_peaks()
     achieved = bv / per_launch / 1e9
@@ -543,7 +598,7 @@ def run_attn(args):
                                                        out=out))
              for kc, vc in caches]
     clocks = ClockSampler(dev)
-    total, per_call = time_calls(calls, K_steps, W, world, per_graph=200)
+    total, per_call = time_calls(calls, K_steps, W, world, per_graph=200, clocks=clocks)
     clk = clocks.stop()
     peak, peak_kind = measured_peaks()
     nbytes = attention_bytes(case)
@@ -606,28 +661,48 @@ def path_table(vq, copies, x, W, world):
             d["rows_per_s"] = rows / per
         out[name] = d
 
+    def record_alternating(arms, rounds=3, n=steps):
+        """Variant arms timed in turn, A/B/A/B..., `rounds` times over; each
+        arm reports the median of its rounds (and the spread)."""
+        per = {name: [] for name in arms}
+        for _ in range(rounds):
+            for name, (calls, _, _) in arms.items():
+                per[name].append(time_calls(calls, n, 20, world)[1])
+        for name, (_, nbytes, rows) in arms.items():
+            med = statistics.median(per[name])
+            out[name] = {"us": med * 1e6, "alg_bytes": nbytes, "gbs": nbytes / med / 1e9,
+                         "rows_per_s": rows / med,
+                         "us_rounds": [round(v * 1e6, 3) for v in per[name]],
+                         "alternation": "A/B/... x%d, median" % rounds}
+
     # narrow output (the pages' N=1024 case) and the block-size / dtype sweep
     w1, c1 = dev_weights(0, n_copies_for(alg_bytes(8, K, 1024)), 1024, K)
+    arms = {}
     for Mi in (4, 8):
         _, xi = dev_act(0, Mi, K, "bf16", 0.5)
         yi = torch.empty((Mi, 1024), dtype=torch.bfloat16, device="cuda")
         wsi = workspace_for(vq, Mi, K, 1024, torch.bfloat16)
-        record("verify_m%d_k5120_n1024_bf16" % Mi,
-               [(lambda c=c, xi=xi, yi=yi, wsi=wsi: vq.vq_linear(xi, *c, y=yi, workspace=wsi))
-                for c in c1], alg_bytes(Mi, K, 1024), rows=Mi)
+        arms["verify_m%d_k5120_n1024_bf16" % Mi] = (
+            [(lambda c=c, xi=xi, yi=yi, wsi=wsi: vq.vq_linear(xi, *c, y=yi, workspace=wsi))
+             for c in c1], alg_bytes(Mi, K, 1024), Mi)
+    record_alternating(arms)
     out["ratio_m8_over_m4_rows_n1024"] = (out["verify_m8_k5120_n1024_bf16"]["rows_per_s"] /
                                           out["verify_m4_k5120_n1024_bf16"]["rows_per_s"])
     del c1
     for dt in ("bf16", "f16", "f32"):
+        arms = {}
         for Mi in (1, 4, 8, 16):
             _, xi = dev_act(0, Mi, K, dt, 0.5)
             yi = torch.empty((Mi, N), dtype=xi.dtype, device="cuda")
             wsi = workspace_for(vq, Mi, K, N, xi.dtype)
             eb = 4 if dt == "f32" else 2
-            record("verify_m%d_k5120_n17408_%s" % (Mi, dt),
-                   [(lambda c=c, xi=xi, yi=yi, wsi=wsi: vq.vq_linear(xi, *c, y=yi, workspace=wsi))
-                    for c in copies],
-                   alg_bytes(Mi, K, N, eb, eb), rows=Mi)
+            arms["verify_m%d_k5120_n17408_%s" % (Mi, dt)] = (
+                [(lambda c=c, xi=xi, yi=yi, wsi=wsi: vq.vq_linear(xi, *c, y=yi, workspace=wsi))
+                 for c in copies], alg_bytes(Mi, K, N, eb, eb), Mi)
+        record_alternating(arms)
+        out["ratio_m16_over_m8_rows_n17408_%s" % dt] = (
+            out["verify_m16_k5120_n17408_%s" % dt]["rows_per_s"] /
+            out["verify_m8_k5120_n17408_%s" % dt]["rows_per_s"])
         out["ratio_m8_over_m4_rows_n17408_%s" % dt] = (
             out["verify_m8_k5120_n17408_%s" % dt]["rows_per_s"] /
             out["verify_m4_k5120_n17408_%s" % dt]["rows_per_s"])
@@ -688,7 +763,30 @@ def path_table(vq, copies, x, W, world):
     return out
 
 
-def cpu_baseline_full(w, xb, budget_s=12.0):
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline_full(w, xb, budget_s=12.0, single_budget_s=6.0):
+    """The oracle on the host cores: the full step with OpenMP over all cores,
+    and single-threaded on a column sample of the same step."""
     import oracle
 
     oracle.build()
@@ -701,10 +799,26 @@ def cpu_baseline_full(w, xb, budget_s=12.0):
         oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16)
     t = time.perf_counter() - t0
     rows = xb.shape[0]
+    n_cols = w.qw.shape[0]
+    # one thread: columns per second on a sample, scaled to rows of the full step
+    sample = np.arange(0, n_cols, 16, dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16, cols=sample, threads=1)
+    t_one = time.perf_counter() - t0
+    reps1 = max(1, int(single_budget_s / max(t_one, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps1):
+        oracle.vq_linear(xb, w.qw, w.scales, w.biases, act_dtype=oracle.BF16, cols=sample,
+                         threads=1)
+    t1 = (time.perf_counter() - t0) / reps1
+    single = rows * (len(sample) / n_cols) / t1
     return {"value": rows * reps / t, "unit": "rows/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": "full M=%d K=5120 N=17408 bf16 step, %d repeats, fp64 scalar C, OpenMP "
-                      "over output columns" % (rows, reps)}
+                      "over output columns" % (rows, reps),
+            "single_thread": {"value": single, "unit": "rows/s", "cores": 1,
+                              "sample": "every 16th output column (%d of %d), %d repeats"
+                                        % (len(sample), n_cols, reps1)}}
 
 
 # ----------------------------------------------------------------------------- reference arm

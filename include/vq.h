@@ -92,12 +92,15 @@ extern "C" {
  *          With the slices, the call enqueues two kernels: the slices, then
  *          the projection, which may start before the slices are done and
  *          waits for them.
- * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 512,
- *          N >= 1. Other K (multiples of 64) return VQ_EUNSUPPORTED, and so do
- *          shapes whose shared-memory plan does not fit: K > 32768 with 8 < M
- *          <= 16; with fp32 x and M > 16, K > 12800; with 16-bit x, M > 16 and
- *          an N narrow enough that K is split (N < 9728 on 152 SMs), K > 16384
- *          for M <= 32 and K > 6144 above. vq_plan() tells whether a shape runs.
+ * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 64,
+ *          N >= 1. K that is not a multiple of 512 runs on the per-stage x
+ *          kernels with a last, partial stage (the scales and biases are then
+ *          read without a tensor map, whose rows must be 16-byte multiples).
+ *          Shapes whose shared-memory plan does not fit return
+ *          VQ_EUNSUPPORTED: K > 32768 with 8 < M <= 16; with fp32 x and
+ *          M > 16, K > 12800; with 16-bit x, M > 16 and an N narrow enough
+ *          that K is split (N < 9728 on 152 SMs), K > 16384 for M <= 32 and
+ *          K > 6144 above. vq_plan() tells whether a shape runs.
  * Accumulation is fp32; each 64-wide group is accumulated from exact integer
  * codes and scaled once, so the only roundings are the fp32 sums and the
  * final cast.
@@ -124,7 +127,7 @@ int vq_linear(const void* x, int M, int K, int N, const uint32_t* qw, const uint
  * workspace: vq_vocab_argmax_workspace_bytes(M) bytes, required, 16-byte
  *          aligned, zero-filled before its first use; every call leaves it
  *          zero-filled again.
- * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 512,
+ * Sizes    1 <= M <= 64 (M <= 32 for VQ_F32), K a positive multiple of 64,
  *          1 <= N < 2^31; as vq_linear, K > 32768 with 8 < M <= 16 and
  *          K > 9728 with fp32 x and M > 16 return VQ_EUNSUPPORTED.
  */
@@ -258,7 +261,7 @@ int kv_compact_per_row(void* const* tensors, int n_tensors, int B, int H, int S_
  *            pointers); all ignored when n_tensors == 0.
  * workspace  verify_round_workspace_bytes(B, L) bytes, 16-byte aligned,
  *            zero-filled before its first use; left zero-filled where needed.
- * Sizes      1 <= B*L <= 64, K a positive multiple of 512, N >= 1. Every
+ * Sizes      1 <= B*L <= 64, K a positive multiple of 64, N >= 1. Every
  *            argument is checked before the first launch.
  */
 size_t verify_round_workspace_bytes(int B, int L);
@@ -268,6 +271,45 @@ int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
                  void* const* kv_tensors, int n_tensors, int H, int S_cap, int D, int elem_bytes,
                  const int32_t* prefix_len, const int32_t* src_off, int32_t* new_len,
                  int32_t* status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * One verify round committing several caches, each with its own geometry.
+ *
+ * Source: mlxcel #2865 "perf(speculative): commit per-row accepts in batched
+ * DFlash", Summary -- besides the target's attention cache, the drafter's
+ * context is still one rectangular prefix shared by the batch, which keeps
+ * the drafter's walk short; the follow-up it records is to give the drafter a
+ * per-row context as well. That is the same per-row commit applied to the
+ * drafter's cache, whose layer count, head count, head size, capacity and
+ * prefix lengths are its own.
+ *
+ * The same operation as verify_round (arg max, fold accept, bonus), then, for
+ * every set i of sets[0..n_sets-1], the per-row commit of kv_compact_per_row
+ * on that set's tensors with its own H, S_cap, D, elem_bytes, prefix_len,
+ * src_off and new_len, and with keep[b] = accept[b] + 1 for every set (the
+ * committed token's slot and the accepted drafts'), max_keep = L.
+ *
+ * sets     HOST array of n_sets descriptors (0 <= n_sets; NULL when 0); each
+ *          descriptor's fields are as kv_compact_per_row's arguments of the
+ *          same names (tensors is a HOST array of DEVICE pointers).
+ * status   optional int32 on the device, shared by every set: bit 0 is OR-ed
+ *          in for any row any set leaves untouched (never cleared).
+ * Other arguments, sizes and the workspace as verify_round. Every argument of
+ * every set is checked before the first launch.
+ */
+typedef struct {
+  void* const* tensors;
+  int32_t n_tensors;
+  int32_t H, S_cap, D, elem_bytes;
+  const int32_t* prefix_len;
+  const int32_t* src_off;
+  int32_t* new_len;
+} vq_kv_set;
+int verify_round_multi(const void* h, int B, int L, int K, int N, const uint32_t* qw,
+                       const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                       const int32_t* tokens, int32_t* target, int32_t* accept, int32_t* bonus,
+                       const vq_kv_set* sets, int n_sets, int32_t* status, void* workspace,
+                       size_t workspace_bytes, void* stream);
 
 /*
  * Attention of the verify block over the per-row KV cache, one layer.

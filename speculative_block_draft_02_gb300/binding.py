@@ -35,6 +35,8 @@ SIGNATURES = {
     "verify_round_workspace_bytes": (_S, [_I, _I]),
     "verify_round": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                           _I, _P, _P, _P, _P, _P, _S, _P]),
+    "verify_round_multi": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _P, _P,
+                                _S, _P]),
     "verify_attention_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I]),
     "verify_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _D, _D,
                               _I, _P, _P, _S, _P]),
@@ -217,6 +219,51 @@ def verify_round(h, qw, scales, biases, tokens, workspace, kv=None, prefix_len=N
                             _stream(stream))
     _check(rc, "verify_round")
     return target, accept, bonus, (new_len if kv else None)
+
+
+class KvSet(ctypes.Structure):
+    """vq_kv_set: one set of caches committed by verify_round_multi."""
+    _fields_ = [("tensors", ctypes.c_void_p), ("n_tensors", ctypes.c_int32),
+                ("H", ctypes.c_int32), ("S_cap", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("elem_bytes", ctypes.c_int32), ("prefix_len", ctypes.c_void_p),
+                ("src_off", ctypes.c_void_p), ("new_len", ctypes.c_void_p)]
+
+
+def verify_round_multi(h, qw, scales, biases, tokens, workspace, sets=(), status=None,
+                       target=None, accept=None, bonus=None, stream=None):
+    """One fold-layout verify round committing several cache sets: (target
+    int32[B][L], accept int32[B], bonus int32[B], [new_len int32[B] per set]).
+    Each set is (kv, prefix_len, src_off): a list of [B][H][S_cap][D] cache
+    tensors of one shape and that set's int32[B] prefix lengths and block
+    offsets (e.g. the target's attention cache and the drafter's context)."""
+    B, L = tokens.shape
+    M, K = h.shape
+    N = qw.shape[0]
+    dev = h.device
+    if target is None:
+        target = torch.empty((B, L), dtype=torch.int32, device=dev)
+    if accept is None:
+        accept = torch.empty(B, dtype=torch.int32, device=dev)
+    if bonus is None:
+        bonus = torch.empty(B, dtype=torch.int32, device=dev)
+    descs = (KvSet * max(1, len(sets)))()
+    keep_alive, new_lens = [], []
+    for i, (kv, prefix_len, src_off) in enumerate(sets):
+        t0 = kv[0]
+        _, H, S_cap, D = t0.shape
+        arr = (ctypes.c_void_p * len(kv))(*[_ptr(t).value for t in kv])
+        keep_alive.append(arr)
+        nl = torch.empty(B, dtype=torch.int32, device=dev)
+        new_lens.append(nl)
+        descs[i] = KvSet(ctypes.cast(arr, ctypes.c_void_p), len(kv), H, S_cap, D,
+                         t0.element_size(), _ptr(prefix_len), _ptr(src_off), _ptr(nl))
+    rc = lib().verify_round_multi(_ptr(h), B, L, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
+                                  _ACT[h.dtype], _ptr(tokens), _ptr(target), _ptr(accept),
+                                  _ptr(bonus), ctypes.cast(descs, ctypes.c_void_p), len(sets),
+                                  _ptr(status), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "verify_round_multi")
+    return target, accept, bonus, new_lens
 
 
 class _Plan(ctypes.Structure):

@@ -1,5 +1,6 @@
 // C-ABI entry points of the W4 projections (vq_linear, vq_vocab_argmax),
 // their host-side planning and tensor-map encoding, and the status calls.
+#include <cstring>
 #include <mutex>
 
 #include "vq_gemm.cuh"
@@ -106,6 +107,7 @@ int red_bytes(int MT) {
 // Shape of one launch: everything but the pointers.
 struct Plan {
   int MT, MP, D, pre, KT, RB, S, n_units, grid;
+  bool sb_plain;    // K % 512 != 0: scales and biases by plain loads (see GemmParams)
   bool red_alias;   // K-slice partials in the stage ring (one unit per block)
   int stage_bytes, off_x, off_s, off_b, xbox_bytes, xm, tab_bytes, xs_stage;
   uint32_t tx_bytes;
@@ -117,7 +119,6 @@ struct Plan {
 int check_shape(int M, int K, int N, int act) {
   if (act != VQ_BF16 && act != VQ_F16 && act != VQ_F32) return VQ_EINVAL;
   if (M < 1 || M > 64 || K < 64 || N < 1 || K % 64 != 0) return VQ_EINVAL;
-  if (K % kBK != 0) return VQ_EUNSUPPORTED;
   if (act == VQ_F32 && M > 32) return VQ_EUNSUPPORTED;
   return VQ_OK;
 }
@@ -139,7 +140,13 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   //         about what two row blocks of the main loop save);
   //  xm = 0 otherwise: x for the stage by TMA, [group][8*MT rows][128 B] with
   //         rows >= M zero-filled, and a table of group sums per block.
-  p.KT = K / kBK;
+  // K not a multiple of 512: a last, partial stage whose groups past K arrive
+  // zero-filled, and scales and biases by plain loads (their rows are then
+  // not the 16-byte multiples a TMA tensor map needs) on the per-stage x
+  // kernels (xm = 0, xm = 3); the x-table and prepared-slice variants take
+  // whole stages only
+  p.KT = (K + kBK - 1) / kBK;
+  p.sb_plain = K % kBK != 0;
   p.RB = (int)(((long long)N + kBN - 1) / kBN);
   p.S = 1;
   if (!argmax && 2 * p.RB < sms) {
@@ -164,7 +171,7 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
     // a table of X_g for all of K if it leaves room for two stages, else
     // X_g per stage from the x tile (two stages' worth, double-buffered)
     const int sb = tc_stage_bytes(p.MP);
-    int tab_tc = (int)round_up((size_t)tc_xs_bytes(K, p.MP), 1024);
+    int tab_tc = (int)round_up((size_t)tc_xs_bytes(p.KT * kBK, p.MP), 1024);
     p.xs_stage = 0;
     if ((kSmemLimit - 1024 - kTcMiscBytes - tab_tc) / sb < 2) {
       p.xs_stage = 1;
@@ -181,7 +188,8 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
       p.off_s = kTcOffS;
       p.off_b = kTcOffB;
       p.xbox_bytes = 128 * p.MP;
-      p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + 8 * 128 * p.MP);
+      p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + (p.sb_plain ? 0 : 2 * kBN * 16) +
+                              8 * 128 * p.MP);
       p.tab_bytes = tab_tc;
       p.red_alias = false;
       p.smem = 1024 + (size_t)D * sb + tab_tc + kTcMiscBytes;
@@ -190,7 +198,7 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
         p.ws_xp_bytes = 0;
         p.ws_bytes = round_up((size_t)M * 8 + 4, 16);
       } else {
-        p.ws_xp_bytes = p.xs_stage ? 0 : round_up((size_t)tc_xs_bytes(K, p.MP), 256);
+        p.ws_xp_bytes = p.xs_stage ? 0 : round_up((size_t)tc_xs_bytes(p.KT * kBK, p.MP), 256);
         p.ws_bytes = p.ws_xp_bytes;
       }
       *pl = p;
@@ -204,14 +212,14 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   const int red = p.red_alias ? 0 : red_bytes(p.MT);
   const long long rb_total = ((long long)N + kBN - 1) / kBN;
   const long long per_block = (rb_total + sms - 1) / sms;
-  const bool mt1_16 = !f32 && p.MT == 1;
+  const bool mt1_16 = !f32 && p.MT == 1 && !p.sb_plain;
   if (mt1_16 && !argmax)
     p.xm = 2;
   else if (mt1_16 && argmax && xt_table_bytes(K) <= kMaxXtBytes && per_block >= 3)
     p.xm = 1;
   else
     p.xm = 0;
-  p.ws_xp_bytes = (p.xm == 2) ? round_up((size_t)(K / kBK) * kSliceBytes, 256) : 0;
+  p.ws_xp_bytes = (p.xm == 2) ? round_up((size_t)p.KT * kSliceBytes, 256) : 0;
   int tab;
   int x_bytes;   // x bytes a stage receives
   if (p.xm == 2) {
@@ -236,7 +244,7 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
     p.off_s = stage_off_s(act, p.MT);
     p.off_b = stage_off_b(act, p.MT);
     p.stage_bytes = stage_bytes(act, p.MT);
-    tab = xsum_bytes(K, p.MT);
+    tab = xsum_bytes(p.KT * kBK, p.MT);
     if (tab > kMaxXsumBytes) return VQ_EUNSUPPORTED;
     x_bytes = n_xbox * p.xbox_bytes;
   }
@@ -248,7 +256,7 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   // before it in the stream. Three measured best for the projection: the
   // first stages' x then queues behind fewer weight bytes.
   p.pre = p.D < 3 ? p.D : 3;
-  p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + 2 * kBN * 16 + x_bytes);
+  p.tx_bytes = (uint32_t)(2 * kWeightBoxBytes + (p.sb_plain ? 0 : 2 * kBN * 16) + x_bytes);
   p.tab_bytes = tab;
   p.smem = 1024 + (size_t)p.D * p.stage_bytes + misc_bytes(argmax) + red + tab;
   // workspace: [prepared x table][split-K counters][split-K partials]
@@ -315,6 +323,9 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
   p.off_b = pl.off_b;
 
   p.tx_bytes = pl.tx_bytes;
+  p.sb_plain = pl.sb_plain ? 1 : 0;
+  p.scales = scales;
+  p.biases = biases;
   p.xm = pl.xm;
   p.xs_stage = pl.xs_stage;
   p.tab_bytes = pl.tab_bytes;
@@ -345,14 +356,21 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
                       (uint64_t)K / 2, 32, kBN, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B)))
     return rc;
-  if ((rc = encode_2d(&L.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)K / 64,
-                      (uint64_t)N, (uint64_t)K / 32, 8, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
-    return rc;
-  if ((rc = encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, (uint64_t)K / 64,
-                      (uint64_t)N, (uint64_t)K / 32, 8, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
-    return rc;
+  if (pl.sb_plain) {
+    // rows of K/32 bytes: no tensor map can describe them; the kernel loads
+    // scales and biases itself and never reads these maps
+    memset(&L.tm_s, 0, sizeof L.tm_s);
+    memset(&L.tm_b, 0, sizeof L.tm_b);
+  } else {
+    if ((rc = encode_2d(&L.tm_s, CU_TENSOR_MAP_DATA_TYPE_UINT16, scales, (uint64_t)K / 64,
+                        (uint64_t)N, (uint64_t)K / 32, 8, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
+      return rc;
+    if ((rc = encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT16, biases, (uint64_t)K / 64,
+                        (uint64_t)N, (uint64_t)K / 32, 8, kBN, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B)))
+      return rc;
+  }
   const int eb = f32 ? 4 : 2;
   // box rows = 8*MT >= M: the rows past M are out of range and arrive zeroed;
   // the x-table variant takes every group of K in one box

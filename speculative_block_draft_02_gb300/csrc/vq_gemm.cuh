@@ -73,19 +73,25 @@ constexpr int kBK = 512;             // k per pipeline stage: 8 groups of 64
 constexpr int kMaxStages = 8;
 constexpr int kWeightBoxBytes = kBN * 128;   // 128 rows x 32 words
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in per block
-// misc area after the stage ring: 2 x 8 mbarriers, flags, arg max scratch
-constexpr int kMiscBytes = 256 + 3 * 8 * 64 * 4;
+// misc area after the stage ring: 3 x 8 mbarriers and one more, flags, arg
+// max scratch
+constexpr int kBarBytes = 320;
+constexpr int kMiscBytes = kBarBytes + 3 * 8 * 64 * 4;
 // bytes of the misc region: the arg max's cross-warp buffers only with ARGMAX
-__host__ __device__ constexpr int misc_bytes(bool argmax) { return argmax ? kMiscBytes : 256; }
+__host__ __device__ constexpr int misc_bytes(bool argmax) { return argmax ? kMiscBytes : kBarBytes; }
 
 // Work split of the consumers by the number MT of n8 tiles (M <= 8*MT):
-// TEAMS teams taking alternate stages, RT 16-row tiles per warp (two tiles
+// TEAMS teams taking alternate stages, RT 16-row tiles per warp (the tiles
 // share the x fragments), KQ K-slices per stage within a team, GPW = 8/KQ
-// groups per warp and stage.
-template <int MT>
+// groups per warp and stage. WIDE (prepared slices, no K split): four row
+// tiles per warp and half the warps, so that each warp has four independent
+// MMA chains and, with 9 warps a block, up to 168 registers (17 warps cap
+// them at 96); measured 11.3 vs 12.0 us per headline call. With a K split,
+// whose units are one or two stages, the narrower split stays faster.
+template <int MT, bool WIDE = false>
 struct Cfg {
   static constexpr int TEAMS = MT <= 2 ? 2 : 1;   // a power of two
-  static constexpr int RT = MT <= 2 ? 2 : 1;
+  static constexpr int RT = (MT == 1 && WIDE) ? 4 : (MT <= 2 ? 2 : 1);
   static constexpr int KQ = MT <= 2 ? 2 : 1;
   static constexpr int GPW = 8 / KQ;
   static constexpr int RW = 8 / RT;                 // warps along the rows
@@ -139,14 +145,15 @@ __host__ __device__ constexpr int xt_prepared_bytes(int K) { return (K / 64) * 1
 __host__ __device__ constexpr int xt_table_bytes(int K) { return xt_prepared_bytes(K) + (K / 64) * 32 + 32; }
 constexpr int kMaxXtBytes = 96 * 1024;
 
-// Bytes of the per-block table of group sums X_g[m]: [K/64][8*MT] fp32.
+// Bytes of the per-block table of group sums X_g[m]: [K/64][8*MT] fp32 (the
+// caller passes K rounded up to whole stages; the groups past K are zero).
 __host__ __device__ constexpr int xsum_bytes(int K, int MT) { return (K / 64) * 8 * MT * 4; }
 constexpr int kMaxXsumBytes = 32 * 1024;
 
 struct GemmParams {
   const void* x;    // activations in global memory (for the group sums)
   int M, K, N;
-  int KT;           // stages along the full K
+  int KT;           // stages along K (the last one partial when K % 512 != 0)
   int S;            // K splits per row block (1 = no split)
   int n_units;      // row blocks * S
   int D;            // pipeline depth (stages in the shared-memory ring)
@@ -164,6 +171,12 @@ struct GemmParams {
                     // (same shared-memory layout either way: [group][8*MT rows][128 B],
                     // rows >= M zero-filled by the copy)
   uint32_t tx_bytes;
+  // K not a multiple of 512 (x per stage by TMA only): the rows of scales and
+  // biases are not 16-byte multiples, which a TMA tensor map needs, so the
+  // producer warp's lanes load each stage's scales and biases themselves
+  int sb_plain;
+  const uint16_t* scales;   // [N][K/64] bf16 bits
+  const uint16_t* biases;
   void* y;
   float* part;                 // split-K partials [S][M][N]
   uint32_t* cnt;               // split-K arrival counters [row blocks]
@@ -191,6 +204,42 @@ int launch_gemm_f16(const GemmLaunch& L);
 int launch_gemm_f32(const GemmLaunch& L);
 
 #ifdef __CUDACC__
+
+// Scales and biases of one stage (128 rows x 8 groups from row block rb,
+// stage kt) with plain loads by the 32 lanes of a warp, rows past N and
+// groups past K as zeros, in the layout the TMA box would leave ([row][8]
+// bf16, 16 B a row); lane l takes rows l + 32i. For K % 512 != 0, whose rows
+// of K/32 bytes no tensor map can describe.
+template <typename Params>
+__device__ __forceinline__ void load_stage_sb(const Params& p, uint8_t* s_dst, uint8_t* b_dst,
+                                              int kt, int rb, int lane) {
+  const int G = p.K / 64;
+  uint4 vs[4], vb[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const long long n = (long long)rb * 128 + lane + 32 * i;
+    uint32_t ws[4] = {0u, 0u, 0u, 0u}, wb[4] = {0u, 0u, 0u, 0u};
+    if (n < p.N) {
+      const unsigned short* ps = reinterpret_cast<const unsigned short*>(p.scales) + n * G;
+      const unsigned short* pb = reinterpret_cast<const unsigned short*>(p.biases) + n * G;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int gi = kt * 8 + j;
+        if (gi < G) {
+          ws[j >> 1] |= (uint32_t)__ldg(ps + gi) << (16 * (j & 1));
+          wb[j >> 1] |= (uint32_t)__ldg(pb + gi) << (16 * (j & 1));
+        }
+      }
+    }
+    vs[i] = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+    vb[i] = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    *reinterpret_cast<uint4*>(s_dst + (lane + 32 * i) * 16) = vs[i];
+    *reinterpret_cast<uint4*>(b_dst + (lane + 32 * i) * 16) = vb[i];
+  }
+}
 
 // A wait that also gives up when another warp of the block already gave up.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
@@ -562,7 +611,7 @@ __device__ __forceinline__ void build_xsum(float* xsum, const GemmParams& p, int
   constexpr int PPW = 32 / CPG;                   // (group, row) pairs per warp step
   constexpr int kBatch = 8;                       // loads in flight per thread
   const int KG = p.K / 64;
-  const int pairs = KG * MP;
+  const int pairs = p.KT * 8 * MP;   // whole stages: groups past K are summed as 0
   const int chunk = lane % CPG;
   const int step = n_warps * PPW;
   const size_t eb = (ACT == VQ_F32) ? 4 : 2;
@@ -573,7 +622,7 @@ __device__ __forceinline__ void build_xsum(float* xsum, const GemmParams& p, int
       const int pair = base + b * step + lane / CPG;
       const int gi = pair / MP, m = pair - (pair / MP) * MP;
       v[b] = make_uint4(0u, 0u, 0u, 0u);
-      if (pair < pairs && m < p.M)
+      if (pair < pairs && m < p.M && gi < KG)
         v[b] = __ldg(reinterpret_cast<const uint4*>(
             static_cast<const uint8_t*>(p.x) + ((size_t)m * p.K + (size_t)gi * 64) * eb +
             chunk * 16));
@@ -889,8 +938,9 @@ struct XsLane {
   uint32_t inv;             // 1/f of rows 2t, 2t+1
 };
 
+template <bool WIDE>
 __device__ __forceinline__ XsLane xs_lane(int rw, int kq, int g, int t) {
-  using C = Cfg<1>;
+  using C = Cfg<1, WIDE>;
   XsLane o;
   const int row = 16 * (C::RT * rw) + 2 * g;
   const int box = (C::GPW == 4) ? kq * kWeightBoxBytes : 0;
@@ -910,10 +960,10 @@ __device__ __forceinline__ XsLane xs_lane(int rw, int kq, int g, int t) {
 // One stage of the prepared-slice variant (MT = 1): the warp's K-slice of
 // groups for its RT row tiles, folded in the stage's scaled units and then
 // brought back with the slice's 1/f.
-template <int ACT>
+template <int ACT, bool WIDE>
 __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
-                                                 float (&tot)[Cfg<1>::RT][1][4]) {
-  using C = Cfg<1>;
+                                                 float (&tot)[Cfg<1, WIDE>::RT][1][4]) {
+  using C = Cfg<1, WIDE>;
   constexpr int RT = C::RT, GPW = C::GPW;
   constexpr int kBiasOff = kBN * 16;
   constexpr uint32_t kMagic16 = 0x64006400u;   // fp16 1024.0 in both halves
@@ -995,12 +1045,12 @@ __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
   }
 }
 
-template <int ACT, int MT, bool ARGMAX, int XM>
-__global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
+template <int ACT, int MT, bool ARGMAX, int XM, bool WIDE = false>
+__global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
     vq_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_x,
                    const GemmParams p) {
-  using C = Cfg<MT>;
+  using C = Cfg<MT, WIDE>;
   constexpr int MP = 8 * MT;
   constexpr int RT = C::RT, KQ = C::KQ, RW = C::RW, TEAMS = C::TEAMS, SLICES = C::SLICES;
   constexpr bool XT = (XM == 1);   // x table built in the block
@@ -1019,11 +1069,11 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   uint8_t* const tabs = sbase + p.D * p.stage_bytes;
   uint8_t* const misc = tabs + p.tab_bytes;
   const uint32_t misc_a = base + p.D * p.stage_bytes + p.tab_bytes;
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 192);
-  volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 196);
-  float* const red_v = reinterpret_cast<float*>(misc + 256);
-  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + 8 * 64 * 4);
-  float* const red_s = reinterpret_cast<float*>(misc + 256 + 2 * 8 * 64 * 4);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 264);
+  volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 268);
+  float* const red_v = reinterpret_cast<float*>(misc + kBarBytes);
+  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + kBarBytes + 8 * 64 * 4);
+  float* const red_s = reinterpret_cast<float*>(misc + kBarBytes + 2 * 8 * 64 * 4);
   float* const red_k = p.red_alias ? reinterpret_cast<float*>(sbase)   // [SLICES-1][128][MP]
                                    : reinterpret_cast<float*>(misc + misc_bytes(ARGMAX));
   float* const xsum = reinterpret_cast<float*>(tabs);   // [K/64][MP]
@@ -1036,6 +1086,9 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   X.rmax = reinterpret_cast<uint32_t*>(X.U + KG * 8);
   auto full_bar = [&](int s) { return misc_a + 8u * s; };
   auto empty_bar = [&](int s) { return misc_a + 64u + 8u * s; };
+  // scales and biases loaded by the producer lanes landed (sb_plain)
+  auto sbfull_bar = [&](int s) { return misc_a + 136u + 8u * s; };
+  const bool sbp = (XM == 0) && p.sb_plain;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the next kernel in the stream may be scheduled as soon as SMs free up
@@ -1045,6 +1098,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     for (int s = 0; s < p.D; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), C::WPT);   // one team consumes each stage
+      if (sbp) mbar_init(sbfull_bar(s), 32);   // every producer lane
     }
     mbar_init(x_bar, 1);
     *abort_flag = 0;
@@ -1057,27 +1111,45 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&tm_w);
-      prefetch_tensormap(&tm_s);
-      prefetch_tensormap(&tm_b);
-      prefetch_tensormap(&tm_x);
+    // lane 0 issues the TMA copies; with sb_plain all 32 lanes also load the
+    // stage's scales and biases (weights too: they may be read before the wait)
+    if (lane == 0 || sbp) {
+      if (lane == 0) {
+        prefetch_tensormap(&tm_w);
+        if (!sbp) {
+          prefetch_tensormap(&tm_s);
+          prefetch_tensormap(&tm_b);
+        }
+        prefetch_tensormap(&tm_x);
+      }
       // Weights are constants of the model: the first stages' weights are
       // requested before waiting for the kernel before this one in the stream
       // (programmatic dependent launch), so the weight stream overlaps that
       // kernel's tail. x, which that kernel may write, is requested only after
       // the wait.
       const uint64_t w_policy = l2_evict_first_policy();
+      auto load_sb = [&](int slot, int kt, int rb) {
+        uint8_t* const st = sbase + slot * p.stage_bytes;
+        load_stage_sb(p, st + p.off_s, st + p.off_b, kt, rb, lane);
+        mbar_arrive(sbfull_bar(slot));
+      };
       auto issue_w = [&](int slot, int kt, int rb) {
         const uint32_t sb = base + slot * p.stage_bytes;
         const uint32_t fb = full_bar(slot);
-        mbar_arrive_expect_tx(fb, p.tx_bytes);
-        tma_load_2d_hint(sb, &tm_w, kt * (kBK / 8), rb * kBN, fb, w_policy);
-        tma_load_2d_hint(sb + kWeightBoxBytes, &tm_w, kt * (kBK / 8) + 32, rb * kBN, fb, w_policy);
-        tma_load_2d_hint(sb + p.off_s, &tm_s, kt * (kBK / 64), rb * kBN, fb, w_policy);
-        tma_load_2d_hint(sb + p.off_b, &tm_b, kt * (kBK / 64), rb * kBN, fb, w_policy);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, p.tx_bytes);
+          tma_load_2d_hint(sb, &tm_w, kt * (kBK / 8), rb * kBN, fb, w_policy);
+          tma_load_2d_hint(sb + kWeightBoxBytes, &tm_w, kt * (kBK / 8) + 32, rb * kBN, fb,
+                           w_policy);
+          if (!sbp) {
+            tma_load_2d_hint(sb + p.off_s, &tm_s, kt * (kBK / 64), rb * kBN, fb, w_policy);
+            tma_load_2d_hint(sb + p.off_b, &tm_b, kt * (kBK / 64), rb * kBN, fb, w_policy);
+          }
+        }
+        if (sbp) load_sb(slot, kt, rb);
       };
       auto issue_x = [&](int slot, int kt) {
+        if (lane != 0) return;
         const uint32_t sb = base + slot * p.stage_bytes;
         const uint32_t fb = full_bar(slot);
         if constexpr (XS) {
@@ -1107,7 +1179,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
       }
       grid_wait_prerequisites();
       bool ok = true;
-      if constexpr (XT) {
+      if (XT && lane == 0) {
         // the block's x, all K/64 groups of 8 rows, first of all
         mbar_arrive_expect_tx(x_bar, (uint32_t)KG * 1024u);
         if (p.x3d) {
@@ -1138,7 +1210,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
           ++q;
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         // let the copies already issued land before the block can exit
         for (int r = (q > p.D ? q - p.D : 0); r < q; ++r)
           wait_bounded(full_bar(r % p.D), (uint32_t)(r / p.D) & 1u, p.err);
@@ -1176,7 +1248,7 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
   uint32_t xsum_a = 0, T_a = 0;
   XsLane xsl;
   if constexpr (XS) {
-    xsl = xs_lane(rw, kq, g, t);
+    xsl = xs_lane<WIDE>(rw, kq, g, t);
   } else if constexpr (XT) {
     if (!wait_or_abort(x_bar, 0u, abort_flag, p.err)) aborted = true;
     build_xtab<ACT>(tabs, X, p, threadIdx.x, kConsumers * 32, kConsumers * 32);
@@ -1209,10 +1281,11 @@ __global__ void __launch_bounds__(Cfg<MT>::THREADS, 1)
     for (int kt = kt0; kt < kt1; ++kt, ++q) {
       if (TEAMS > 1 && (q & (TEAMS - 1)) != team) continue;   // the other team's stage
       const uint32_t ph = (uint32_t)phase;
-      const bool ok = !aborted && wait_or_abort(full_bar(slot), ph, abort_flag, p.err);
+      bool ok = !aborted && wait_or_abort(full_bar(slot), ph, abort_flag, p.err);
+      if (sbp) ok = ok && wait_or_abort(sbfull_bar(slot), ph, abort_flag, p.err);
       if (ok) {
         if constexpr (XS)
-          consume_stage_xs<ACT>(base + slot * p.stage_bytes, xsl, tot);
+          consume_stage_xs<ACT, WIDE>(base + slot * p.stage_bytes, xsl, tot);
         else if constexpr (XT)
           consume_stage_xt<ACT>(base + slot * p.stage_bytes, kt, T_a, xl, tot);
         else
@@ -1429,9 +1502,9 @@ int launch_pdl(Kern k, dim3 grid, int threads, size_t smem, cudaStream_t stream,
   return cudaLaunchKernelEx(&cfg, k, args...) == cudaSuccess ? VQ_OK : VQ_ECUDA;
 }
 
-template <int ACT, int MT, bool AM, int XM = 0>
+template <int ACT, int MT, bool AM, int XM = 0, bool WIDE = false>
 int launch_one(const GemmLaunch& L) {
-  auto k = vq_gemm_kernel<ACT, MT, AM, XM>;
+  auto k = vq_gemm_kernel<ACT, MT, AM, XM, WIDE>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem) !=
       cudaSuccess)
     return VQ_ECUDA;
@@ -1441,7 +1514,7 @@ int launch_one(const GemmLaunch& L) {
                               L.p.x, L.p.M, L.p.K, (uint8_t*)L.p.xprep);
     if (rc != VQ_OK) return rc;
   }
-  return launch_pdl(k, dim3(L.grid), Cfg<MT>::THREADS, L.smem, L.stream, L.tm_w, L.tm_s, L.tm_b,
+  return launch_pdl(k, dim3(L.grid), Cfg<MT, WIDE>::THREADS, L.smem, L.stream, L.tm_w, L.tm_s, L.tm_b,
                     L.tm_x, L.p);
 }
 
@@ -1469,7 +1542,7 @@ int launch_gemm_act(const GemmLaunch& L) {
     }
     if (L.p.xm == 2) {
       if (L.MT != 1 || L.argmax) return VQ_EUNSUPPORTED;
-      return launch_one<ACT, 1, false, 2>(L);
+      return L.p.S == 1 ? launch_one<ACT, 1, false, 2, true>(L) : launch_one<ACT, 1, false, 2>(L);
     }
     if (L.p.xm == 3) {
       switch (L.MT) {

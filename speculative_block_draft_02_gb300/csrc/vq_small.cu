@@ -171,15 +171,15 @@ extern "C" size_t verify_round_workspace_bytes(int B, int L) {
   return vq_vocab_argmax_workspace_bytes(B * L) + (((size_t)B * 4 + 15) & ~(size_t)15);
 }
 
-extern "C" int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
-                            const uint16_t* scales, const uint16_t* biases, int act_dtype,
-                            const int32_t* tokens, int32_t* target, int32_t* accept,
-                            int32_t* bonus, void* const* kv_tensors, int n_tensors, int H,
-                            int S_cap, int D, int elem_bytes, const int32_t* prefix_len,
-                            const int32_t* src_off, int32_t* new_len, int32_t* status,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+extern "C" int verify_round_multi(const void* h, int B, int L, int K, int N, const uint32_t* qw,
+                                  const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                                  const int32_t* tokens, int32_t* target, int32_t* accept,
+                                  int32_t* bonus, const vq_kv_set* sets, int n_sets,
+                                  int32_t* status, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
   if (B < 1 || L < 1 || (long long)B * L > 64) return VQ_EINVAL;
   if (!tokens || !target || !accept || !bonus) return VQ_EINVAL;
+  if (n_sets < 0 || (n_sets > 0 && !sets)) return VQ_EINVAL;
   if (((uintptr_t)tokens | (uintptr_t)target | (uintptr_t)accept | (uintptr_t)bonus) & 3u)
     return VQ_EALIGN;
   const size_t need = verify_round_workspace_bytes(B, L);
@@ -187,11 +187,12 @@ extern "C" int verify_round(const void* h, int B, int L, int K, int N, const uin
   if ((uintptr_t)workspace & 15u) return VQ_EALIGN;
   const size_t wa = vq_vocab_argmax_workspace_bytes(B * L);
   int32_t* keep = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + wa);
-  KvTensors tp;
-  if (n_tensors > 0) {
-    // every argument is checked before the first launch
-    const int rc = kv_check(kv_tensors, n_tensors, B, H, S_cap, D, elem_bytes, prefix_len,
-                            src_off, keep, L, new_len, status, &tp);
+  // every argument of every set is checked before the first launch
+  for (int i = 0; i < n_sets; ++i) {
+    const vq_kv_set& c = sets[i];
+    KvTensors tp;
+    const int rc = kv_check(c.tensors, c.n_tensors, B, c.H, c.S_cap, c.D, c.elem_bytes,
+                            c.prefix_len, c.src_off, keep, L, c.new_len, status, &tp);
     if (rc) return rc;
   }
   int rc = vq_vocab_argmax(h, B * L, K, N, qw, scales, biases, act_dtype, target, nullptr,
@@ -202,8 +203,33 @@ extern "C" int verify_round(const void* h, int B, int L, int K, int N, const uin
   fold_accept_kernel<<<blocks, threads, 0, (cudaStream_t)stream>>>(tokens, target, B, L, accept,
                                                                    bonus, keep);
   if (cudaGetLastError() != cudaSuccess) return VQ_ECUDA;
-  if (n_tensors > 0)
-    return kv_compact_per_row(kv_tensors, n_tensors, B, H, S_cap, D, elem_bytes, prefix_len,
-                              src_off, keep, L, new_len, status, stream);
+  for (int i = 0; i < n_sets; ++i) {
+    const vq_kv_set& c = sets[i];
+    rc = kv_compact_per_row(c.tensors, c.n_tensors, B, c.H, c.S_cap, c.D, c.elem_bytes,
+                            c.prefix_len, c.src_off, keep, L, c.new_len, status, stream);
+    if (rc) return rc;
+  }
   return VQ_OK;
+}
+
+extern "C" int verify_round(const void* h, int B, int L, int K, int N, const uint32_t* qw,
+                            const uint16_t* scales, const uint16_t* biases, int act_dtype,
+                            const int32_t* tokens, int32_t* target, int32_t* accept,
+                            int32_t* bonus, void* const* kv_tensors, int n_tensors, int H,
+                            int S_cap, int D, int elem_bytes, const int32_t* prefix_len,
+                            const int32_t* src_off, int32_t* new_len, int32_t* status,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  vq_kv_set set;
+  set.tensors = kv_tensors;
+  set.n_tensors = n_tensors;
+  set.H = H;
+  set.S_cap = S_cap;
+  set.D = D;
+  set.elem_bytes = elem_bytes;
+  set.prefix_len = prefix_len;
+  set.src_off = src_off;
+  set.new_len = new_len;
+  return verify_round_multi(h, B, L, K, N, qw, scales, biases, act_dtype, tokens, target, accept,
+                            bonus, &set, n_tensors > 0 ? 1 : 0, status, workspace,
+                            workspace_bytes, stream);
 }

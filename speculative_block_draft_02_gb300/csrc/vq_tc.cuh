@@ -240,17 +240,19 @@ __device__ __forceinline__ float tc_group_sum_smem(uint32_t tile, int j, int m) 
   return s;
 }
 
-// X_g for the projection, once per call: thread e -> (g, m) = (e / MP, e % MP).
+// X_g for the projection, once per call: thread e -> (g, m) = (e / MP, e % MP),
+// for the groups of KT whole stages (those past K are 0).
 template <int ACT>
 __global__ void __launch_bounds__(256)
-    vq_tc_xsum_kernel(const void* __restrict__ x, int M, int K, int MP, float* __restrict__ out) {
+    vq_tc_xsum_kernel(const void* __restrict__ x, int M, int K, int KT, int MP,
+                      float* __restrict__ out) {
   grid_launch_dependents();
   // x and the table may still be in use by the kernel before this one
   grid_wait_prerequisites();
   const int e = blockIdx.x * 256 + threadIdx.x;
-  if (e >= (K / 64) * MP) return;
+  if (e >= KT * 8 * MP) return;
   const int g = e / MP, m = e - g * MP;
-  out[e] = m < M ? tc_group_sum<ACT>(x, K, m, g) : 0.f;
+  out[e] = (m < M && g < K / 64) ? tc_group_sum<ACT>(x, K, m, g) : 0.f;
 }
 
 // Stage layout: [codes 2 x 16 KiB][scales 128 x 16 B][biases 128 x 16 B][x 8 x MP x 128 B]
@@ -259,8 +261,9 @@ constexpr int kTcOffB = kTcOffS + kBN * 16;
 constexpr int kTcOffX = kTcOffB + kBN * 16;   // 36864: 1 KiB aligned
 __host__ __device__ constexpr int tc_stage_bytes(int MP) { return kTcOffX + 8 * MP * 128; }
 __host__ __device__ constexpr int tc_xs_bytes(int K, int MP) { return (K / 64) * MP * 4; }
-// misc: mbarriers and flags (256 B), arg max scratch [4][64] value, index, runner-up
-constexpr int kTcMiscBytes = 256 + 3 * 4 * 64 * 4;
+// misc: mbarriers and flags (320 B), arg max scratch [4][64] value, index, runner-up
+constexpr int kTcBarBytes = 320;
+constexpr int kTcMiscBytes = kTcBarBytes + 3 * 4 * 64 * 4;
 
 // Best row, its value and the runner-up value over the warp's 32 rows for each
 // of its HC columns, by halving: at offset o (16, 8, ...) a lane keeps the
@@ -334,9 +337,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(misc + 232);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 240);
   volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 244);
-  float* const red_v = reinterpret_cast<float*>(misc + 256);
-  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + 256 + 4 * 64 * 4);
-  float* const red_s = reinterpret_cast<float*>(misc + 256 + 2 * 4 * 64 * 4);
+  // scales and biases loaded by the producer lanes landed (sb_plain)
+  auto sbfull_bar = [&](int s) { return misc_a + 256u + 8u * s; };
+  float* const red_v = reinterpret_cast<float*>(misc + kTcBarBytes);
+  uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + kTcBarBytes + 4 * 64 * 4);
+  float* const red_s = reinterpret_cast<float*>(misc + kTcBarBytes + 2 * 4 * 64 * 4);
+  const bool sbp = p.sb_plain != 0;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the next kernel in the stream may be scheduled as soon as SMs free up
@@ -345,6 +351,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int s = 0; s < p.D; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), kTcFoldWarps);
+      if (sbp) mbar_init(sbfull_bar(s), 32);   // every producer lane
     }
     for (int b = 0; b < kTcBufs; ++b) {
       mbar_init(afull_bar(b), kTcUnpackWarps / 2);
@@ -366,24 +373,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == kTcProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&tm_w);
-      prefetch_tensormap(&tm_s);
-      prefetch_tensormap(&tm_b);
-      prefetch_tensormap(&tm_x);
+    // lane 0 issues the TMA copies; with sb_plain (K % 512 != 0) all 32 lanes
+    // also load the stage's scales and biases
+    if (lane == 0 || sbp) {
+      if (lane == 0) {
+        prefetch_tensormap(&tm_w);
+        if (!sbp) {
+          prefetch_tensormap(&tm_s);
+          prefetch_tensormap(&tm_b);
+        }
+        prefetch_tensormap(&tm_x);
+      }
       // weights (constants of the model) before the wait for the kernel
       // before this one in the stream; x and X_g only after it
       const uint64_t w_policy = l2_evict_first_policy();
       auto issue_w = [&](int slot, int kt, int rb) {
         const uint32_t sb = base + slot * p.stage_bytes;
         const uint32_t fb = full_bar(slot);
-        mbar_arrive_expect_tx(fb, p.tx_bytes);
-        tma_load_2d_hint(sb, &tm_w, kt * (kBK / 8), rb * kBN, fb, w_policy);
-        tma_load_2d_hint(sb + kWeightBoxBytes, &tm_w, kt * (kBK / 8) + 32, rb * kBN, fb, w_policy);
-        tma_load_2d_hint(sb + kTcOffS, &tm_s, kt * (kBK / 64), rb * kBN, fb, w_policy);
-        tma_load_2d_hint(sb + kTcOffB, &tm_b, kt * (kBK / 64), rb * kBN, fb, w_policy);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, p.tx_bytes);
+          tma_load_2d_hint(sb, &tm_w, kt * (kBK / 8), rb * kBN, fb, w_policy);
+          tma_load_2d_hint(sb + kWeightBoxBytes, &tm_w, kt * (kBK / 8) + 32, rb * kBN, fb,
+                           w_policy);
+          if (!sbp) {
+            tma_load_2d_hint(sb + kTcOffS, &tm_s, kt * (kBK / 64), rb * kBN, fb, w_policy);
+            tma_load_2d_hint(sb + kTcOffB, &tm_b, kt * (kBK / 64), rb * kBN, fb, w_policy);
+          }
+        }
+        if (sbp) {
+          load_stage_sb(p, sbase + slot * p.stage_bytes + kTcOffS,
+                        sbase + slot * p.stage_bytes + kTcOffB, kt, rb, lane);
+          mbar_arrive(sbfull_bar(slot));
+        }
       };
       auto issue_x = [&](int slot, int kt) {
+        if (lane != 0) return;
         const uint32_t sb = base + slot * p.stage_bytes;
         const uint32_t fb = full_bar(slot);
         if (p.x3d) {
@@ -401,8 +425,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ++pre;
         }
       grid_wait_prerequisites();
-      if (!ARGMAX && !p.xs_stage) {
-        const uint32_t xs_bytes = (uint32_t)tc_xs_bytes(p.K, MP);
+      if (!ARGMAX && !p.xs_stage && lane == 0) {
+        const uint32_t xs_bytes = (uint32_t)tc_xs_bytes(p.KT * kBK, MP);
         mbar_arrive_expect_tx(xs_bar, xs_bytes);
         bulk_load(smem_addr(xs_tab), p.xprep, xs_bytes, xs_bar);
       }
@@ -428,9 +452,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       // let every copy issued land before the block can exit
-      for (int r = (q > p.D ? q - p.D : 0); r < q; ++r)
-        wait_bounded(full_bar(r % p.D), (uint32_t)(r / p.D) & 1u, p.err);
-      if (!ARGMAX && !p.xs_stage) wait_bounded(xs_bar, 0u, p.err);
+      if (lane == 0) {
+        for (int r = (q > p.D ? q - p.D : 0); r < q; ++r)
+          wait_bounded(full_bar(r % p.D), (uint32_t)(r / p.D) & 1u, p.err);
+        if (!ARGMAX && !p.xs_stage) wait_bounded(xs_bar, 0u, p.err);
+      }
     }
   } else if (warp >= kTcMmaWarp) {
     // ------------------------------------------------------------- MMA issue
@@ -581,6 +607,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           xs_base = dst;
         }
         uint4 sv = make_uint4(0u, 0u, 0u, 0u), bv = sv;
+        if (sbp && !aborted &&
+            !wait_or_abort(sbfull_bar(slot), (uint32_t)(q / p.D) & 1u, abort_flag, p.err))
+          aborted = true;
         if (!aborted) {
           sv = lds128_at(sb + kTcOffS + (uint32_t)nl * 16u);
           bv = lds128_at(sb + kTcOffB + (uint32_t)nl * 16u);
@@ -714,9 +743,9 @@ int launch_tc(const GemmLaunch& L) {
       cudaSuccess)
     return VQ_ECUDA;
   if (!AM && !L.p.xs_stage) {
-    const int n = (L.p.K / 64) * MP;
+    const int n = L.p.KT * 8 * MP;
     const int rc = launch_pdl(vq_tc_xsum_kernel<ACT>, dim3((n + 255) / 256), 256, 0, L.stream,
-                              L.p.x, L.p.M, L.p.K, MP, (float*)L.p.xprep);
+                              L.p.x, L.p.M, L.p.K, L.p.KT, MP, (float*)L.p.xprep);
     if (rc != VQ_OK) return rc;
   }
   return launch_pdl(k, dim3(L.grid), kTcThreads, L.smem, L.stream, L.tm_w, L.tm_s, L.tm_b, L.tm_x,

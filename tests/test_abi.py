@@ -70,11 +70,11 @@ def test_vocab_workspace_size(vqlib):
 def test_host_validation_rejects_before_any_launch(vqlib):
     P = ctypes.c_void_p
     fake = P(0x1000)  # never dereferenced: every call below fails validation first
-    # M out of range, K not a multiple of 64, K not a multiple of 512, bad dtype
+    # M out of range, K not a multiple of 64, bad dtype
     assert vqlib.vq_linear(fake, 0, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
     assert vqlib.vq_linear(fake, 65, 512, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
     assert vqlib.vq_linear(fake, 8, 100, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
-    assert vqlib.vq_linear(fake, 8, 576, 16, fake, fake, fake, fake, 0, None, 0, None) == -4
+    assert vqlib.vq_linear(fake, 8, 544, 16, fake, fake, fake, fake, 0, None, 0, None) == -1
     assert vqlib.vq_linear(fake, 8, 512, 16, fake, fake, fake, fake, 7, None, 0, None) == -1
     assert vqlib.vq_linear(fake, 33, 512, 16, fake, fake, fake, fake, 2, None, 0, None) == -4
     # null and misaligned pointers

@@ -490,3 +490,82 @@ def test_verify_round_fold_layout(B, L, K, N, layers):
         assert np.array_equal(new_len.cpu().numpy(), r_len)
         for d, rr in zip(kv, ref):
             assert np.array_equal(d.cpu().numpy(), rr.view(np.int16))
+
+
+def test_verify_round_commits_the_drafter_context_too():
+    """Per-row drafter context: one round commits the target's attention cache
+    and the drafter's context cache, each with its own layers, heads, head
+    size, capacity, prefix lengths and block offset, both with keep = accept
+    + 1 -- against the oracle composed the same way (fold accept, then the
+    per-row commit of each set)."""
+    B, L, K, N = 4, 16, 512, 20000
+    M = B * L
+    w = synth.w4_weights(404, N, K)
+    hx = synth.activations(404, M, K, "bf16", name="hidden")
+    logits = oracle_linear(hx, w, "bf16")
+    r_target = oracle.argmax(logits)[0].reshape(B, L)
+    r = np.random.default_rng(404)
+    tokens = np.empty((B, L), dtype=np.int32)
+    tokens[:, 0] = r.integers(0, N, size=B)
+    tokens[:, 1:] = synth.drafts_from_target(404, r_target[:, :-1], N)
+    r_acc, r_bonus, r_keep = oracle.fold_accept(tokens, r_target)
+    # the target's cache: 2 layers x {K, V} of [4][2][512][64] fp16, verify
+    # block at the shared offset max(prefix); the drafter's: 1 layer x {K, V}
+    # of [4][4][1024][128], its own (shorter) prefixes, block right after the
+    # longest of them, and one row whose block sits right after its prefix
+    tgt = synth.commit_case(405, layers=2, B=B, H=2, S_cap=512, D=64, block=L, prefix_lo=20,
+                            prefix_hi=400, keep=r_keep, name="target_kv")
+    dft = synth.commit_case(406, layers=1, B=B, H=4, S_cap=1024, D=128, block=L, prefix_lo=5,
+                            prefix_hi=300, keep=r_keep, name="drafter_kv")
+    dft.src_off[2] = dft.prefix_len[2]
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    sets, devs = [], []
+    for case in (tgt, dft):
+        kv = _kv_to_dev(case.tensors)
+        devs.append(kv)
+        sets.append((kv, i32(case.prefix_len), i32(case.src_off)))
+    ws = torch.zeros(vq.verify_round_workspace_bytes(B, L), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    target, acc, bonus, new_lens = vq.verify_round_multi(
+        to_dev_act(hx, "bf16"), *to_dev_weights(w), torch.from_numpy(tokens).cuda(), ws,
+        sets=sets, status=status)
+    torch.cuda.synchronize()
+    assert np.array_equal(target.cpu().numpy(), r_target)
+    assert np.array_equal(acc.cpu().numpy(), r_acc)
+    assert np.array_equal(bonus.cpu().numpy(), r_bonus)
+    assert int(status.item()) == 0
+    for case, kv, nl in zip((tgt, dft), devs, new_lens):
+        ref = [t.copy() for t in case.tensors]
+        r_len, r_status = oracle.kv_compact(ref, case.prefix_len, case.src_off, r_keep, L)
+        assert r_status == 0
+        assert np.array_equal(nl.cpu().numpy(), r_len)
+        for d, rr in zip(kv, ref):
+            assert np.array_equal(d.cpu().numpy(), rr.view(np.int16))
+
+
+# K a multiple of 64 but not of 512: a last stage of 1..7 groups (zero-filled
+# past K), scales and biases loaded without a tensor map; the mma.sync kernel
+# (M <= 16, fp32 x, K splits) and the tcgen05 kernel (16-bit x, M > 16)
+GENERAL_K = [(8, 576, 17408, "bf16"), (16, 576, 3000, "f16"), (64, 576, 17408, "bf16"),
+             (8, 2880, 5000, "bf16"), (16, 2880, 17408, "bf16"), (64, 2880, 12000, "f16"),
+             (8, 5184, 17408, "bf16"), (16, 5184, 9000, "f16"), (64, 5184, 17408, "bf16"),
+             (7, 2880, 1000, "f32"), (8, 5184, 1024, "bf16"), (33, 576, 10001, "bf16"),
+             (3, 64, 300, "bf16")]
+
+
+@pytest.mark.parametrize("M,K,N,dtype", GENERAL_K)
+def test_linear_k_multiple_of_64(M, K, N, dtype):
+    seed = 3 * M + K + N
+    w = synth.w4_weights(seed, N, K)
+    x = synth.activations(seed, M, K, dtype)
+    assert_proj_close(run_linear(x, w, dtype), oracle_linear(x, w, dtype), dtype)
+
+
+@pytest.mark.parametrize("M,K,N", [(8, 576, 20000), (64, 2880, 30000), (64, 5184, 12000),
+                                   (16, 5184, 4000)])
+def test_vocab_argmax_k_multiple_of_64(M, K, N):
+    w = synth.w4_weights(M + K, N, K)
+    x = synth.activations(M + K, M, K, "bf16")
+    idx, mx, ws = run_vocab(x, w)
+    assert check_argmax(idx, mx, oracle_linear(x, w, "bf16")) == 0
+    assert not ws.any(), "workspace must be left zeroed"

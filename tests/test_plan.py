@@ -108,10 +108,29 @@ def test_plan_invariants(vq, act, argmax):
                     assert act != torch.float32 and M > 16 and p["k_splits"] == 1
 
 
+@pytest.mark.parametrize("K", [64, 576, 2880, 5184])
+def test_k_multiple_of_64_runs_on_the_per_stage_x_kernels(vq, K):
+    # a last stage of 1..7 groups; scales and biases by plain loads, so such
+    # shapes run on the per-stage x kernels (mma.sync, or tcgen05 for 16-bit
+    # x with M > 16 and no K split), with or without a K split
+    for M, act, argmax, N in ((8, torch.bfloat16, False, 17408), (16, torch.float16, False, 4096),
+                              (64, torch.bfloat16, False, 17408), (8, torch.bfloat16, True, 151936),
+                              (64, torch.bfloat16, True, 151936), (7, torch.float32, False, 1000),
+                              (8, torch.bfloat16, False, 1024), (24, torch.float16, False, 12000)):
+        p = plan(vq, M, K, N, act, argmax)
+        if M > 16 and act != torch.float32 and p["k_splits"] == 1:
+            assert p["kernel"] == 3
+        else:
+            assert p["kernel"] == 0 and p["launches"] == 1
+        assert p["k_splits"] <= -(-K // 512)
+        assert p["units"] == -(-N // 128) * p["k_splits"]
+        assert p["smem_bytes"] <= LIMIT and p["stages"] >= 2
+
+
 def test_plan_rejects_bad_shapes(vq):
     from speculative_block_draft_02_gb300.binding import VQError
 
-    for args in ((0, 512, 16), (65, 512, 16), (8, 100, 16), (8, 512, 0)):
+    for args in ((0, 512, 16), (65, 512, 16), (8, 100, 16), (8, 512, 0), (8, 544, 16)):
         with pytest.raises(VQError):
             plan(vq, *args)
     with pytest.raises(VQError):
