@@ -154,7 +154,9 @@ def code_only(text: str) -> str:
             j = text.find("*/", i + 2)
             i = n if j < 0 else j + 2
             out.append(" ")
-        elif c in "\"'":
+        elif c == '"' or (c == "'" and not (i > 0 and text[i - 1].isalnum())):
+            # a quote after a letter or digit is a C++14 digit separator
+            # (1'000), not the start of a character literal
             j = i + 1
             while j < n and text[j] != c:
                 j += 2 if text[j] == "\\" else 1

@@ -28,6 +28,11 @@
  *   - Row-major layouts throughout; sizes are in elements unless noted.
  *   - A workspace may be shared by successive calls on one stream, never by
  *     calls that can run at the same time.
+ *   - Set-up: the first call of any projection entry point (vq_linear,
+ *     vq_vocab_argmax and their variants, verify_round*) on a device, with
+ *     that device current, looks up the library's device symbols and the
+ *     driver's tensor-map encoder; make that first call before any stream
+ *     capture on that device.
  *   - vq_linear, vq_vocab_argmax and vq_vocab_argmax_noalloc launch their
  *     kernels with programmatic stream serialization, so that back-to-back
  *     projections overlap: a kernel may start while the kernel before it in
@@ -172,10 +177,12 @@ int vq_vocab_argmax_top2(const void* x, int M, int K, int N, const uint32_t* qw,
  * hands out none for scratch.
  *
  * Limit: 1 <= M <= 64 (the array's size); a larger M returns VQ_EINVAL.
- * Set-up: the first call on a device (with that device current) looks up the
- * array's device address; make that first call before any stream capture.
+ * Set-up: the first call on a device (with that device current) also looks
+ * up the array's device address (see the common set-up rule above).
  * The array is held by every GPU that loads the library until the process
- * exits. Each call clears the part it uses on `stream` before the kernel.
+ * exits. Each call clears the part it uses on `stream` before the kernel
+ * (a completed call leaves it zeroed already; only a call that gave up on a
+ * bounded wait leaves keys behind).
  * Calls share the one array: calls that can overlap on the GPU (different
  * streams, or different host threads) race and must not be made.
  */

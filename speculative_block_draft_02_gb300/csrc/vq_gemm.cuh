@@ -91,7 +91,7 @@ __host__ __device__ constexpr int misc_bytes(bool argmax) { return argmax ? kMis
 template <int MT, bool WIDE = false>
 struct Cfg {
   static constexpr int TEAMS = MT <= 2 ? 2 : 1;   // a power of two
-  static constexpr int RT = (MT == 1 && WIDE) ? 4 : (MT <= 2 ? 2 : 1);
+  static constexpr int RT = (MT <= 2 && WIDE) ? 4 : (MT <= 2 ? 2 : 1);
   static constexpr int KQ = MT <= 2 ? 2 : 1;
   static constexpr int GPW = 8 / KQ;
   static constexpr int RW = 8 / RT;                 // warps along the rows
@@ -414,9 +414,9 @@ struct LaneOffsets {
   uint32_t xs;              // (first group of the slice, row 2t) in the group-sum table, bytes
 };
 
-template <int ACT, int MT>
+template <int ACT, int MT, bool WIDE>
 __device__ __forceinline__ LaneOffsets<ACT, MT> lane_offsets(int rw, int kq, int g, int t) {
-  using C = Cfg<MT>;
+  using C = Cfg<MT, WIDE>;
   constexpr int MP = 8 * MT;
   LaneOffsets<ACT, MT> o;
   const int row = 16 * (C::RT * rw) + 2 * g;               // even row of tile 0
@@ -461,11 +461,11 @@ __device__ __forceinline__ Packed<GPW> lds_packed_at(uint32_t a) {
 // weight row 16r + 2i + 1. sb is the stage's shared address, xsb the group-sum
 // table's shared address for the stage's first group. All per-tile, per-group
 // and per-row offsets are load immediates.
-template <int ACT, int MT>
+template <int ACT, int MT, bool WIDE>
 __device__ __forceinline__ void consume_stage(uint32_t sb, uint32_t xsb,
                                               const LaneOffsets<ACT, MT>& o,
-                                              float (&tot)[Cfg<MT>::RT][MT][4]) {
-  using C = Cfg<MT>;
+                                              float (&tot)[Cfg<MT, WIDE>::RT][MT][4]) {
+  using C = Cfg<MT, WIDE>;
   constexpr int RT = C::RT, GPW = C::GPW, MP = 8 * MT;
   constexpr bool kF16 = (ACT == VQ_F16);
   constexpr bool kF32 = (ACT == VQ_F32);
@@ -1257,7 +1257,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
   } else {
     build_xsum<ACT, MT>(xsum, p, warp, lane, kConsumers);
     named_bar_sync(1, kConsumers * 32);
-    lo = lane_offsets<ACT, MT>(rw, kq, g, t);
+    lo = lane_offsets<ACT, MT, WIDE>(rw, kq, g, t);
     xsum_a = smem_addr(xsum) + lo.xs;
   }
 
@@ -1289,7 +1289,8 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
         else if constexpr (XT)
           consume_stage_xt<ACT>(base + slot * p.stage_bytes, kt, T_a, xl, tot);
         else
-          consume_stage<ACT, MT>(base + slot * p.stage_bytes, xsum_a + kt * (8 * MP * 4), lo, tot);
+          consume_stage<ACT, MT, WIDE>(base + slot * p.stage_bytes, xsum_a + kt * (8 * MP * 4), lo,
+                                       tot);
       } else {
         aborted = true;
       }
@@ -1526,6 +1527,9 @@ template <int ACT>
 int launch_gemm_act(const GemmLaunch& L) {
 #define VQ_CASE(mt)                                                      \
   case mt:                                                               \
+    if (mt <= 2 && L.p.S == 1)                                           \
+      return L.argmax ? launch_one<ACT, mt, true, 0, (mt <= 2)>(L)        \
+                      : launch_one<ACT, mt, false, 0, (mt <= 2)>(L);      \
     return L.argmax ? launch_one<ACT, mt, true>(L) : launch_one<ACT, mt, false>(L);
   if constexpr (ACT == VQ_F32) {
     switch (L.MT) {

@@ -22,6 +22,14 @@ def test_code_only_strips_comments_but_not_strings():
     assert out.endswith("x = y;")
 
 
+def test_code_only_digit_separators_are_not_character_literals():
+    a = "int n = 1'000; // count\nint m = 2;\n"
+    b = "int n = 1'000; /* other */ int m = 2;"
+    out = bench.code_only(a)
+    assert "count" not in out and out == bench.code_only(b)
+    assert out == "int n = 1'000; int m = 2;"
+
+
 def test_code_only_ignores_layout_and_comments_only():
     a = "template <int D>\n__global__ void k(float* p) {\n  p[0] = D;  // store\n}\n"
     b = "template <int D> __global__ void k(float* p) { /* note */ p[0] = D; }"
