@@ -88,9 +88,10 @@ extern "C" {
  *          accumulator; fp32 output for VQ_F32), 4-byte aligned.
  * workspace / workspace_bytes
  *          scratch for (a) x converted once per call into per-stage slices of
- *          scaled fp16 MMA fragments (16-bit x with M <= 8: about 17.6*K
- *          bytes), and (b) the split-K reduction used when N is too narrow to
- *          fill the GPU. vq_linear_workspace_bytes() gives the size needed (0
+ *          scaled fp16 MMA fragments (16-bit x with M <= 16 and K a multiple
+ *          of 512: about 17.6*K bytes per 8 rows), (b) the group row sums of x
+ *          (16-bit x, M > 16), and (c) the split-K reduction used when N is
+ *          too narrow to fill the GPU. vq_linear_workspace_bytes() gives the size needed (0
  *          when neither is used; then workspace may be NULL). The workspace
  *          must be zero-filled before its first use; every call leaves the
  *          part that must start at zero zero-filled again. 16-byte aligned.
@@ -102,10 +103,11 @@ extern "C" {
  *          kernels with a last, partial stage (the scales and biases are then
  *          read without a tensor map, whose rows must be 16-byte multiples).
  *          Shapes whose shared-memory plan does not fit return
- *          VQ_EUNSUPPORTED: K > 32768 with 8 < M <= 16; with fp32 x and
- *          M > 16, K > 12800; with 16-bit x, M > 16 and an N narrow enough
- *          that K is split (N < 9728 on 152 SMs), K > 16384 for M <= 32 and
- *          K > 6144 above. vq_plan() tells whether a shape runs.
+ *          VQ_EUNSUPPORTED: K > 32768 with fp32 x and 8 < M <= 16, or with
+ *          K not a multiple of 512 and 8 < M <= 16; with fp32 x and M > 16,
+ *          K > 12800; with 16-bit x, M > 16 and an N narrow enough that K is
+ *          split (N < 9728 on 152 SMs), K > 16384 for M <= 32 and K > 6144
+ *          above. vq_plan() tells whether a shape runs.
  * Accumulation is fp32; each 64-wide group is accumulated from exact integer
  * codes and scaled once, so the only roundings are the fp32 sums and the
  * final cast.

@@ -58,17 +58,67 @@ int device_state(int* sms, int32_t** err) {
   return VQ_OK;
 }
 
+// Encoded tensor maps, cached per host thread: a verify step calls the same
+// projections on the same weights every time, and cuTensorMapEncodeTiled is a
+// driver call per map, four per call. A map depends only on what the key
+// holds (address, type, sizes, strides, box, swizzle), never on the contents,
+// so a buffer freed and allocated again at the same address reuses its map.
+struct TmKey {
+  const void* ptr;
+  int32_t dev, dt, rank, sw, l2, pad;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+};
+struct TmEntry {
+  TmKey key;
+  CUtensorMap map;
+};
+constexpr int kTmCache = 64;
+thread_local TmEntry t_tm[kTmCache];
+thread_local int t_tm_used = 0, t_tm_next = 0;
+
+int encode(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int rank,
+           const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+           CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
+  TmKey k;
+  memset(&k, 0, sizeof k);   // the padding takes part in the comparison
+  k.ptr = ptr;
+  if (cudaGetDevice(&k.dev) != cudaSuccess) return VQ_ECUDA;
+  k.dt = (int32_t)dt;
+  k.rank = rank;
+  k.sw = (int32_t)sw;
+  k.l2 = (int32_t)l2;
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+  }
+  for (int i = 0; i + 1 < rank; ++i) k.strides[i] = strides[i];
+  for (int i = 0; i < t_tm_used; ++i) {
+    if (memcmp(&t_tm[i].key, &k, sizeof k) == 0) {
+      *m = t_tm[i].map;
+      return VQ_OK;
+    }
+  }
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, dt, (cuuint32_t)rank, const_cast<void*>(ptr), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return VQ_ECUDA;
+  TmEntry& e = t_tm[t_tm_next];
+  e.key = k;
+  e.map = *m;
+  t_tm_next = (t_tm_next + 1) % kTmCache;
+  if (t_tm_used < kTmCache) ++t_tm_used;
+  return VQ_OK;
+}
+
 int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
               CUtensorMapSwizzle sw, CUtensorMapL2promotion l2) {
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, l2,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? VQ_OK : VQ_ECUDA;
+  return encode(m, dt, ptr, 2, dims, strides, box, sw, l2);
 }
 
 // x viewed as [K/inner][M][inner] (group-major), so one box brings a stage's
@@ -81,12 +131,8 @@ int encode_x3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int M, i
   const cuuint64_t dims[3] = {inner, (cuuint64_t)M, (cuuint64_t)K / inner};
   const cuuint64_t strides[2] = {(cuuint64_t)K * elem_bytes, 128};
   const cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)box_rows, (cuuint32_t)box_groups};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? VQ_OK : VQ_ECUDA;
+  return encode(m, dt, ptr, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
 }
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -132,9 +178,9 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   const bool f32 = act == VQ_F32;
   const int n_xbox = f32 ? 16 : 8;
   // Where x comes from:
-  //  xm = 2 (vq_linear, 16-bit x, M <= 8): slices of scaled fp16 fragments
-  //         prepared by a small kernel before the projection, one per stage,
-  //         copied into the stage next to its weights;
+  //  xm = 2 (vq_linear, 16-bit x, M <= 16): slices of scaled fp16
+  //         fragments prepared by a small kernel before the projection, one
+  //         per stage and n8 tile, copied into the stage next to its weights;
   //  xm = 1 (arg max, 16-bit x, M <= 8, several row blocks per block): the
   //         block converts all of x once into a table (the conversion costs
   //         about what two row blocks of the main loop save);
@@ -213,13 +259,13 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
   const long long rb_total = ((long long)N + kBN - 1) / kBN;
   const long long per_block = (rb_total + sms - 1) / sms;
   const bool mt1_16 = !f32 && p.MT == 1 && !p.sb_plain;
-  if (mt1_16 && !argmax)
+  if (!f32 && p.MT <= 2 && !p.sb_plain && !argmax)
     p.xm = 2;
   else if (mt1_16 && argmax && xt_table_bytes(K) <= kMaxXtBytes && per_block >= 3)
     p.xm = 1;
   else
     p.xm = 0;
-  p.ws_xp_bytes = (p.xm == 2) ? round_up((size_t)p.KT * kSliceBytes, 256) : 0;
+  p.ws_xp_bytes = (p.xm == 2) ? round_up((size_t)p.KT * p.MT * kSliceBytes, 256) : 0;
   int tab;
   int x_bytes;   // x bytes a stage receives
   if (p.xm == 2) {
@@ -227,9 +273,9 @@ int make_plan(int M, int K, int N, int act, bool argmax, int sms, Plan* pl) {
     p.off_x = xs_stage_off_x();
     p.off_s = xt_stage_off_s();
     p.off_b = xt_stage_off_s() + kBN * 16;
-    p.stage_bytes = xs_stage_bytes();
+    p.stage_bytes = xs_stage_bytes(p.MT);
     tab = 0;
-    x_bytes = kSliceBytes;
+    x_bytes = p.MT * kSliceBytes;
   } else if (p.xm == 1) {
     p.xbox_bytes = 0;
     p.off_x = 0;

@@ -430,9 +430,7 @@ int attn_launch(const AttnParams& p, int B, cudaStream_t stream) {
   const size_t smem = (size_t)(kAttnRows + kChunk) * (D + 8) * 2 + (size_t)D * (kChunk + 8) * 2 +
                       (size_t)p.L * p.rot_half * sizeof(float2);
   auto* partial = verify_attn_partial_kernel<kF16, D>;
-  if (cudaFuncSetAttribute(partial, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return VQ_ECUDA;
+  if (ensure_smem<verify_attn_partial_kernel<kF16, D>>(smem) != VQ_OK) return VQ_ECUDA;
   partial<<<dim3(p.NC, p.Hkv * p.RG, B), kAttnThreads, smem, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return VQ_ECUDA;
   // the merge may be scheduled while the partial kernel runs; it waits for it

@@ -226,6 +226,26 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
 }  // namespace vq
 
 // ---------------------------------------------------------------- host side
+#include <atomic>
+
 namespace vq {
 int num_sms_current_device(int* out);
+
+// Raises kernel K's dynamic shared-memory limit on the current device to at
+// least `bytes`, calling the runtime only the first time a device needs a
+// larger limit (the attribute persists; per call it would cost a driver call).
+template <auto K>
+int ensure_smem(size_t bytes) {
+  static std::atomic<int> set[64];   // per device: the largest limit set so far
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VQ_ECUDA;
+  if ((int)bytes <= set[dev].load(std::memory_order_relaxed)) return VQ_OK;
+  if (cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return VQ_ECUDA;
+  int cur = set[dev].load(std::memory_order_relaxed);
+  while ((int)bytes > cur && !set[dev].compare_exchange_weak(cur, (int)bytes)) {
+  }
+  return VQ_OK;
+}
 }  // namespace vq

@@ -133,9 +133,12 @@ constexpr int kSliceT = 8 * 1024;
 constexpr int kSliceU = kSliceT + 8 * 8 * 4;
 constexpr int kSliceInv = kSliceU + 8 * 4 * 16;
 constexpr int kSliceBytes = kSliceInv + 8 * 4;
+// With M <= 16 (two n8 tiles) a stage holds one slice per tile, tile mt's
+// at xs_stage_off_x() + mt * kSliceBytes (slice-local rows 0..7 = x rows
+// 8mt .. 8mt + 7).
 __host__ __device__ constexpr int xs_stage_off_x() { return 2 * kWeightBoxBytes + 2 * kBN * 16; }
-__host__ __device__ constexpr int xs_stage_bytes() {
-  return (xs_stage_off_x() + kSliceBytes + 1023) / 1024 * 1024;
+__host__ __device__ constexpr int xs_stage_bytes(int MT = 1) {
+  return (xs_stage_off_x() + MT * kSliceBytes + 1023) / 1024 * 1024;
 }
 
 // x table [K/64 groups][8 rows][128 B] fp16, then T [K/64][8] fp32 and 1/f [8]
@@ -852,16 +855,17 @@ __device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T
 // the f-scaled group sums T, -U and 1/f. Each slice is prepared once per call.
 template <int ACT>
 __device__ __forceinline__ void prep_slice_row(const void* __restrict__ x, int M, int K, int kt,
-                                               int m, int lane, uint8_t* __restrict__ slice) {
+                                               int xm_row, int lane, uint8_t* __restrict__ slice) {
+  const int m = xm_row & 7;   // the row within the slice
   uint4 v[2];
   float mx = 0.f, gs[2];
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
     const int ci = lane + 32 * b;   // chunk of 8 values: group ci/8, position ci%8
     v[b] = make_uint4(0u, 0u, 0u, 0u);
-    if (m < M)
-      v[b] = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(x) +
-                                                  ((size_t)m * K + (size_t)kt * kBK + ci * 8) * 2));
+    if (xm_row < M)
+      v[b] = __ldg(reinterpret_cast<const uint4*>(
+          static_cast<const uint8_t*>(x) + ((size_t)xm_row * K + (size_t)kt * kBK + ci * 8) * 2));
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -911,20 +915,21 @@ __device__ __forceinline__ void prep_slice_row(const void* __restrict__ x, int M
   if (lane == 0) reinterpret_cast<float*>(slice + kSliceInv)[m] = 1.f / f;
 }
 
-// The slices of one call: block kt prepares stage kt, one row per warp. It is
-// launched so that it may start while the kernel before it in the stream is
-// finishing, and waits for that kernel before it reads x or overwrites the
-// slices; the projection after it waits for it in the same way.
-constexpr int kPrepThreads = 256;   // 8 warps: the 8 rows of a stage
+// The slices of one call, [KT stages][MT tiles]: block b prepares stage
+// b / MT, tile b % MT, one row per warp. It is launched so that it may start
+// while the kernel before it in the stream is finishing, and waits for that
+// kernel before it reads x or overwrites the slices; the projection after it
+// waits for it in the same way.
+constexpr int kPrepThreads = 256;   // 8 warps: the 8 rows of a tile
 
 template <int ACT>
 __global__ void __launch_bounds__(kPrepThreads)
-    vq_prep_kernel(const void* __restrict__ x, int M, int K, uint8_t* __restrict__ out) {
+    vq_prep_kernel(const void* __restrict__ x, int M, int K, int MT, uint8_t* __restrict__ out) {
   grid_launch_dependents();
   grid_wait_prerequisites();
-  const int kt = blockIdx.x;
-  prep_slice_row<ACT>(x, M, K, kt, threadIdx.x >> 5, threadIdx.x & 31,
-                      out + (size_t)kt * kSliceBytes);
+  const int kt = blockIdx.x / MT, mt = blockIdx.x - (blockIdx.x / MT) * MT;
+  prep_slice_row<ACT>(x, M, K, kt, 8 * mt + (threadIdx.x >> 5), threadIdx.x & 31,
+                      out + (size_t)blockIdx.x * kSliceBytes);
 }
 
 // Per-thread constants of the prepared-slice consumer (offsets in a stage).
@@ -938,9 +943,9 @@ struct XsLane {
   uint32_t inv;             // 1/f of rows 2t, 2t+1
 };
 
-template <bool WIDE>
+template <int MT, bool WIDE>
 __device__ __forceinline__ XsLane xs_lane(int rw, int kq, int g, int t) {
-  using C = Cfg<1, WIDE>;
+  using C = Cfg<MT, WIDE>;
   XsLane o;
   const int row = 16 * (C::RT * rw) + 2 * g;
   const int box = (C::GPW == 4) ? kq * kWeightBoxBytes : 0;
@@ -957,17 +962,19 @@ __device__ __forceinline__ XsLane xs_lane(int rw, int kq, int g, int t) {
   return o;
 }
 
-// One stage of the prepared-slice variant (MT = 1): the warp's K-slice of
-// groups for its RT row tiles, folded in the stage's scaled units and then
-// brought back with the slice's 1/f.
-template <int ACT, bool WIDE>
+// One stage of the prepared-slice variant (MT n8 tiles, one slice each):
+// the warp's K-slice of groups for its RT row tiles, folded in each slice's
+// scaled units and then brought back with the slice's 1/f. The codes are
+// unpacked once per row tile and serve every n8 tile.
+template <int ACT, int MT, bool WIDE>
 __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
-                                                 float (&tot)[Cfg<1, WIDE>::RT][1][4]) {
-  using C = Cfg<1, WIDE>;
+                                                 float (&tot)[Cfg<MT, WIDE>::RT][MT][4]) {
+  using C = Cfg<MT, WIDE>;
   constexpr int RT = C::RT, GPW = C::GPW;
   constexpr int kBiasOff = kBN * 16;
   constexpr uint32_t kMagic16 = 0x64006400u;   // fp16 1024.0 in both halves
   static_assert(GPW == 4 || GPW == 8, "K-slices of 4 or 8 groups");
+  static_assert(MT == 1 || MT == 2, "one or two n8 tiles");
 
   Packed<GPW> sc0[RT], sc1[RT], bi0[RT], bi1[RT];
   const uint32_t sa = sb + o.sc;
@@ -981,9 +988,11 @@ __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
   const uint32_t we = sb + o.w_even, wo = sb + o.w_odd;
   const uint32_t xa0 = sb + o.x_h0, xa1 = sb + o.x_h1;
   const uint32_t ta = sb + o.ts;
-  float part[RT][4];
+  float part[RT][MT][4];
 #pragma unroll
-  for (int r = 0; r < RT; ++r) part[r][0] = part[r][1] = part[r][2] = part[r][3] = 0.f;
+  for (int r = 0; r < RT; ++r)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) part[r][mt][0] = part[r][mt][1] = part[r][mt][2] = part[r][mt][3] = 0.f;
 
   static_for<GPW>([&](auto jc) {
     constexpr int jj = decltype(jc)::value;
@@ -996,13 +1005,21 @@ __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
       wa[r] = lds64<kBox + 2048 * r>(ae);
       wb[r] = lds64<kBox + 2048 * r>(ao);
     });
-    const uint4 nuv = lds128<jj * 64>(sb + o.nu);
-    const float4 nu = make_float4(__uint_as_float(nuv.x), __uint_as_float(nuv.y),
-                                  __uint_as_float(nuv.z), __uint_as_float(nuv.w));
-    float acc[RT][4];
+    float4 nu[MT];
+    static_for<MT>([&](auto mc) {
+      constexpr int mt = decltype(mc)::value;
+      const uint4 nuv = lds128<jj * 64 + mt * kSliceBytes>(sb + o.nu);
+      nu[mt] = make_float4(__uint_as_float(nuv.x), __uint_as_float(nuv.y), __uint_as_float(nuv.z),
+                           __uint_as_float(nuv.w));
+    });
+    float acc[RT][MT][4];
     static_for<2>([&](auto hc) {
       constexpr int h = decltype(hc)::value;
-      const uint4 bx = lds128<jj * 1024>(h ? xa1 : xa0);
+      uint4 bx[MT];
+      static_for<MT>([&](auto mc) {
+        constexpr int mt = decltype(mc)::value;
+        bx[mt] = lds128<jj * 1024 + mt * kSliceBytes>(h ? xa1 : xa0);
+      });
 #pragma unroll
       for (int r = 0; r < RT; ++r) {
         const uint32_t qa = h ? wa[r].y : wa[r].x;
@@ -1014,35 +1031,44 @@ __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
                                 lop3_and_or(qa, 0x00F000F0u, kMagic16), lop3_and_or(qb, 0x00F000F0u, kMagic16)};
         const uint32_t a1[4] = {lop3_and_or(qa8, 0x000F000Fu, kMagic16), lop3_and_or(qb8, 0x000F000Fu, kMagic16),
                                 lop3_and_or(qa8, 0x00F000F0u, kMagic16), lop3_and_or(qb8, 0x00F000F0u, kMagic16)};
-        float (&d)[4] = acc[r];
-        if (h == 0)
-          mma_16816_c<true>(d, a0, bx.x, bx.y, nu);
-        else
-          mma_16816<true>(d, a0, bx.x, bx.y);
-        mma_16816<true>(d, a1, bx.z, bx.w);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          float (&d)[4] = acc[r][mt];
+          if (h == 0)
+            mma_16816_c<true>(d, a0, bx[mt].x, bx[mt].y, nu[mt]);
+          else
+            mma_16816<true>(d, a0, bx[mt].x, bx[mt].y);
+          mma_16816<true>(d, a1, bx[mt].z, bx[mt].w);
+        }
       }
     });
-    const uint2 tv = lds64<jj * 32>(ta);
-    const float T0 = __uint_as_float(tv.x), T1 = __uint_as_float(tv.y);
+    static_for<MT>([&](auto mc) {
+      constexpr int mt = decltype(mc)::value;
+      const uint2 tv = lds64<jj * 32 + mt * kSliceBytes>(ta);
+      const float T0 = __uint_as_float(tv.x), T1 = __uint_as_float(tv.y);
+#pragma unroll
+      for (int r = 0; r < RT; ++r) {
+        const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
+        const float b_a = bf16_of(bi0[r], jj), b_b = bf16_of(bi1[r], jj);
+        part[r][mt][0] = fmaf(s_a, acc[r][mt][0], fmaf(b_a, T0, part[r][mt][0]));
+        part[r][mt][1] = fmaf(s_a, acc[r][mt][1], fmaf(b_a, T1, part[r][mt][1]));
+        part[r][mt][2] = fmaf(s_b, acc[r][mt][2], fmaf(b_b, T0, part[r][mt][2]));
+        part[r][mt][3] = fmaf(s_b, acc[r][mt][3], fmaf(b_b, T1, part[r][mt][3]));
+      }
+    });
+  });
+  static_for<MT>([&](auto mc) {
+    constexpr int mt = decltype(mc)::value;
+    const uint2 iv = lds64<mt * kSliceBytes>(sb + o.inv);
+    const float i0 = __uint_as_float(iv.x), i1 = __uint_as_float(iv.y);
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
-      const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
-      const float b_a = bf16_of(bi0[r], jj), b_b = bf16_of(bi1[r], jj);
-      part[r][0] = fmaf(s_a, acc[r][0], fmaf(b_a, T0, part[r][0]));
-      part[r][1] = fmaf(s_a, acc[r][1], fmaf(b_a, T1, part[r][1]));
-      part[r][2] = fmaf(s_b, acc[r][2], fmaf(b_b, T0, part[r][2]));
-      part[r][3] = fmaf(s_b, acc[r][3], fmaf(b_b, T1, part[r][3]));
+      tot[r][mt][0] = fmaf(i0, part[r][mt][0], tot[r][mt][0]);
+      tot[r][mt][1] = fmaf(i1, part[r][mt][1], tot[r][mt][1]);
+      tot[r][mt][2] = fmaf(i0, part[r][mt][2], tot[r][mt][2]);
+      tot[r][mt][3] = fmaf(i1, part[r][mt][3], tot[r][mt][3]);
     }
   });
-  const uint2 iv = lds64<0>(sb + o.inv);
-  const float i0 = __uint_as_float(iv.x), i1 = __uint_as_float(iv.y);
-#pragma unroll
-  for (int r = 0; r < RT; ++r) {
-    tot[r][0][0] = fmaf(i0, part[r][0], tot[r][0][0]);
-    tot[r][0][1] = fmaf(i1, part[r][1], tot[r][0][1]);
-    tot[r][0][2] = fmaf(i0, part[r][2], tot[r][0][2]);
-    tot[r][0][3] = fmaf(i1, part[r][3], tot[r][0][3]);
-  }
 }
 
 template <int ACT, int MT, bool ARGMAX, int XM, bool WIDE = false>
@@ -1153,8 +1179,9 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
         const uint32_t sb = base + slot * p.stage_bytes;
         const uint32_t fb = full_bar(slot);
         if constexpr (XS) {
-          bulk_load(sb + p.off_x, static_cast<const uint8_t*>(p.xprep) + (size_t)kt * kSliceBytes,
-                    kSliceBytes, fb);
+          bulk_load(sb + p.off_x,
+                    static_cast<const uint8_t*>(p.xprep) + (size_t)kt * MT * kSliceBytes,
+                    MT * kSliceBytes, fb);
         } else if constexpr (XT) {
           // x comes from the block's table
         } else if (p.x3d) {
@@ -1248,7 +1275,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
   uint32_t xsum_a = 0, T_a = 0;
   XsLane xsl;
   if constexpr (XS) {
-    xsl = xs_lane<WIDE>(rw, kq, g, t);
+    xsl = xs_lane<MT, WIDE>(rw, kq, g, t);
   } else if constexpr (XT) {
     if (!wait_or_abort(x_bar, 0u, abort_flag, p.err)) aborted = true;
     build_xtab<ACT>(tabs, X, p, threadIdx.x, kConsumers * 32, kConsumers * 32);
@@ -1285,7 +1312,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
       if (sbp) ok = ok && wait_or_abort(sbfull_bar(slot), ph, abort_flag, p.err);
       if (ok) {
         if constexpr (XS)
-          consume_stage_xs<ACT, WIDE>(base + slot * p.stage_bytes, xsl, tot);
+          consume_stage_xs<ACT, MT, WIDE>(base + slot * p.stage_bytes, xsl, tot);
         else if constexpr (XT)
           consume_stage_xt<ACT>(base + slot * p.stage_bytes, kt, T_a, xl, tot);
         else
@@ -1380,6 +1407,38 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
         if (*epi_flag) {
           __threadfence();
           if (!aborted) {
+            // the slices are added in slice order (deterministic); every
+            // element of the thread and four slices at a time are loaded
+            // together, so the sum costs a few L2 round trips, not S per element
+            const size_t slice_stride = (size_t)p.M * p.N;
+            float acc[RT][MT][4];
+#pragma unroll
+            for (int r = 0; r < RT; ++r)
+#pragma unroll
+              for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[r][mt][e] = 0.f;
+            for (int k0 = 0; k0 < p.S; k0 += 4) {
+#pragma unroll
+              for (int r = 0; r < RT; ++r)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
+                    const int m = 8 * mt + 2 * t + (e & 1);
+                    if (n < p.N && m < p.M) {
+                      const float* src = p.part + ((size_t)k0 * p.M + m) * p.N + n;
+                      float v[4];
+#pragma unroll
+                      for (int i = 0; i < 4; ++i)
+                        v[i] = k0 + i < p.S ? __ldcg(src + i * slice_stride) : 0.f;
+#pragma unroll
+                      for (int i = 0; i < 4; ++i)
+                        if (k0 + i < p.S) acc[r][mt][e] += v[i];
+                    }
+                  }
+            }
 #pragma unroll
             for (int r = 0; r < RT; ++r)
 #pragma unroll
@@ -1388,12 +1447,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
                 for (int e = 0; e < 4; ++e) {
                   const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
                   const int m = 8 * mt + 2 * t + (e & 1);
-                  if (n < p.N && m < p.M) {
-                    float s = 0.f;
-                    for (int k = 0; k < p.S; ++k)
-                      s += __ldcg(p.part + ((size_t)k * p.M + m) * p.N + n);
-                    store_out<ACT>(p.y, (size_t)m * p.N + n, s);
-                  }
+                  if (n < p.N && m < p.M) store_out<ACT>(p.y, (size_t)m * p.N + n, acc[r][mt][e]);
                 }
           }
           if (threadIdx.x == 0) p.cnt[rb] = 0u;
@@ -1506,13 +1560,11 @@ int launch_pdl(Kern k, dim3 grid, int threads, size_t smem, cudaStream_t stream,
 template <int ACT, int MT, bool AM, int XM = 0, bool WIDE = false>
 int launch_one(const GemmLaunch& L) {
   auto k = vq_gemm_kernel<ACT, MT, AM, XM, WIDE>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem) !=
-      cudaSuccess)
-    return VQ_ECUDA;
+  if (ensure_smem<vq_gemm_kernel<ACT, MT, AM, XM, WIDE>>(L.smem) != VQ_OK) return VQ_ECUDA;
   if constexpr (XM == 2 && ACT != VQ_F32) {
     // the slices first; the projection may start before they are done
-    const int rc = launch_pdl(vq_prep_kernel<ACT>, dim3(L.p.KT), kPrepThreads, 0, L.stream,
-                              L.p.x, L.p.M, L.p.K, (uint8_t*)L.p.xprep);
+    const int rc = launch_pdl(vq_prep_kernel<ACT>, dim3(L.p.KT * MT), kPrepThreads, 0, L.stream,
+                              L.p.x, L.p.M, L.p.K, MT, (uint8_t*)L.p.xprep);
     if (rc != VQ_OK) return rc;
   }
   return launch_pdl(k, dim3(L.grid), Cfg<MT, WIDE>::THREADS, L.smem, L.stream, L.tm_w, L.tm_s, L.tm_b,
@@ -1545,7 +1597,9 @@ int launch_gemm_act(const GemmLaunch& L) {
       return launch_one<ACT, 1, true, 1>(L);
     }
     if (L.p.xm == 2) {
-      if (L.MT != 1 || L.argmax) return VQ_EUNSUPPORTED;
+      if (L.MT > 2 || L.argmax) return VQ_EUNSUPPORTED;
+      if (L.MT == 2)
+        return L.p.S == 1 ? launch_one<ACT, 2, false, 2, true>(L) : launch_one<ACT, 2, false, 2>(L);
       return L.p.S == 1 ? launch_one<ACT, 1, false, 2, true>(L) : launch_one<ACT, 1, false, 2>(L);
     }
     if (L.p.xm == 3) {

@@ -149,11 +149,7 @@ extern "C" int kv_compact_per_row(void* const* tensors, int n_tensors, int B, in
   const long long buf_bytes = (long long)max_keep * slot_bytes;
   const long long blocks = (long long)n_tensors * B * H;
   const size_t smem = (size_t)(buf_bytes > 0 ? buf_bytes : 16);
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(kv_compact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
-      return VQ_ECUDA;
-  }
+  if (smem > 48 * 1024 && ensure_smem<kv_compact_kernel>(smem) != VQ_OK) return VQ_ECUDA;
   kv_compact_kernel<<<(unsigned)blocks, 256, smem, (cudaStream_t)stream>>>(
       tp, B, H, S_cap, (int)(slot_bytes / 16), prefix_len, src_off, keep, max_keep, new_len,
       status);

@@ -739,9 +739,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 template <int ACT, int MP, bool AM>
 int launch_tc(const GemmLaunch& L) {
   auto k = vq_tc_kernel<ACT, MP, AM>;
-  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem) !=
-      cudaSuccess)
-    return VQ_ECUDA;
+  if (ensure_smem<vq_tc_kernel<ACT, MP, AM>>(L.smem) != VQ_OK) return VQ_ECUDA;
   if (!AM && !L.p.xs_stage) {
     const int n = L.p.KT * 8 * MP;
     const int rc = launch_pdl(vq_tc_xsum_kernel<ACT>, dim3((n + 255) / 256), 256, 0, L.stream,

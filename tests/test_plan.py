@@ -39,7 +39,11 @@ def test_next_block_verify_runs_on_tcgen05(vq):
 
 
 def test_small_m_and_fp32_stay_on_mma_sync(vq):
-    assert plan(vq, 16, 5120, 17408)["kernel"] == 0
+    # 16-bit x with M <= 16: prepared slices, one per n8 tile (two at M = 16)
+    p = plan(vq, 16, 5120, 17408)
+    assert p["kernel"] == 2 and p["launches"] == 2 and p["stages"] == 4
+    assert p["workspace_bytes"] == -(-10 * 2 * SLICE // 256) * 256
+    assert plan(vq, 16, 5120, 17408, argmax=True)["kernel"] == 0
     assert plan(vq, 8, 5120, 17408, torch.float32)["kernel"] == 0
     assert plan(vq, 32, 512, 17408, torch.float32)["kernel"] == 0
 
@@ -59,7 +63,8 @@ def test_long_k_sums_the_x_groups_per_stage(vq):
     with pytest.raises(Exception):
         plan(vq, 64, 6656, 1024)              # K split at M > 32
     with pytest.raises(Exception):
-        plan(vq, 16, 33280, 17408)
+        plan(vq, 16, 33280, 151936, argmax=True)
+    assert plan(vq, 16, 33280, 17408)["kernel"] == 2     # prepared slices: any K
     with pytest.raises(Exception):
         plan(vq, 32, 13312, 17408, torch.float32)
 
