@@ -161,6 +161,9 @@ struct GemmParams {
   int n_units;      // row blocks * S
   int D;            // pipeline depth (stages in the shared-memory ring)
   int pre;          // stages whose weights are requested before griddepcontrol.wait
+  // SM clock cycles between those requests while the kernel before this one
+  // is still running (0: all at once)
+  int pace;
   int red_alias;    // 1: the K-slice partials live in the stage ring (one unit per block)
   int stage_bytes;
   int off_x, off_s, off_b;   // offsets inside a stage (codes at 0)
@@ -1097,6 +1100,8 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
   const uint32_t misc_a = base + p.D * p.stage_bytes + p.tab_bytes;
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(misc + 264);
   volatile int* const epi_flag = reinterpret_cast<volatile int*>(misc + 268);
+  // set once the consumers' griddepcontrol.wait has returned
+  volatile int* const dep_flag = reinterpret_cast<volatile int*>(misc + 272);
   float* const red_v = reinterpret_cast<float*>(misc + kBarBytes);
   uint32_t* const red_i = reinterpret_cast<uint32_t*>(misc + kBarBytes + 8 * 64 * 4);
   float* const red_s = reinterpret_cast<float*>(misc + kBarBytes + 2 * 8 * 64 * 4);
@@ -1128,6 +1133,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
     }
     mbar_init(x_bar, 1);
     *abort_flag = 0;
+    *dep_flag = 0;
     if constexpr (XT) {
       for (int i = 0; i < 8; ++i) X.rmax[i] = 0u;
     }
@@ -1199,7 +1205,17 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
         const int rb = u0 / p.S, sp = u0 - rb * p.S;
         const int kt0 = sp * p.KT / p.S, kt1 = (sp + 1) * p.KT / p.S;
         kt_first = kt0;
+        // The requests are spaced while the kernel before this one runs: the
+        // memory system then holds a short queue of weight requests rather
+        // than megabytes of them, and the small reads that come right after
+        // the wait (that kernel's successor reading x, this kernel's slices)
+        // are not stuck behind it. The spacing stops once the consumers have
+        // seen the wait return, so a call with nothing before it is not slowed.
+        const long long t_pace = clock64();
         for (int r = 0; r < p.pre && r < p.D && kt0 + r < kt1; ++r) {
+          if (r > 0)
+            while (!*dep_flag && clock64() - t_pace < (long long)r * p.pace) {
+            }
           issue_w(r, kt0 + r, rb);
           ++pre;
         }
@@ -1268,6 +1284,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
   bool aborted = false;
   // x and every output may belong to the kernel before this one in the stream
   grid_wait_prerequisites();
+  if (threadIdx.x == 0) *dep_flag = 1;
   // group sums of x (or the whole x table) for all of K, while the first
   // stages are in flight
   LaneOffsets<ACT, MT> lo;
@@ -1371,7 +1388,8 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
     }
 
     if constexpr (!ARGMAX) {
-      if (p.S == 1) {
+      // (the WIDE layout is only launched without a K split)
+      if (WIDE || p.S == 1) {
         if (!aborted) {
 #pragma unroll
           for (int r = 0; r < RT; ++r)
@@ -1407,9 +1425,13 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
         if (*epi_flag) {
           __threadfence();
           if (!aborted) {
-            // the slices are added in slice order (deterministic); every
-            // element of the thread and four slices at a time are loaded
-            // together, so the sum costs a few L2 round trips, not S per element
+            // the slices are added in slice order (deterministic). Every load
+            // of a round (all elements of the thread, KB slices) is issued
+            // before any is used: the addresses of elements outside y and of
+            // slices past S are clamped to valid ones and their values
+            // dropped, so no load sits behind a branch and the sum costs
+            // ceil(S / KB) L2 round trips rather than one per element.
+            constexpr int KB = (RT * MT <= 2) ? 4 : 2;
             const size_t slice_stride = (size_t)p.M * p.N;
             float acc[RT][MT][4];
 #pragma unroll
@@ -1418,26 +1440,33 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
               for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[r][mt][e] = 0.f;
-            for (int k0 = 0; k0 < p.S; k0 += 4) {
+            for (int k0 = 0; k0 < p.S; k0 += KB) {
+              float v[RT][MT][4][KB];
 #pragma unroll
-              for (int r = 0; r < RT; ++r)
+              for (int i = 0; i < KB; ++i) {
+                const float* sl = p.part + (size_t)(k0 + i < p.S ? k0 + i : p.S - 1) * slice_stride;
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
+                for (int r = 0; r < RT; ++r)
 #pragma unroll
-                  for (int e = 0; e < 4; ++e) {
-                    const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
-                    const int m = 8 * mt + 2 * t + (e & 1);
-                    if (n < p.N && m < p.M) {
-                      const float* src = p.part + ((size_t)k0 * p.M + m) * p.N + n;
-                      float v[4];
+                  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                      for (int i = 0; i < 4; ++i)
-                        v[i] = k0 + i < p.S ? __ldcg(src + i * slice_stride) : 0.f;
-#pragma unroll
-                      for (int i = 0; i < 4; ++i)
-                        if (k0 + i < p.S) acc[r][mt][e] += v[i];
+                    for (int e = 0; e < 4; ++e) {
+                      const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
+                      const int m = 8 * mt + 2 * t + (e & 1);
+                      const bool in = n < p.N && m < p.M;
+                      v[r][mt][e][i] = __ldcg(sl + (in ? (size_t)m * p.N + n : 0));
                     }
-                  }
+              }
+#pragma unroll
+              for (int i = 0; i < KB; ++i)
+                if (k0 + i < p.S) {
+#pragma unroll
+                  for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                      for (int e = 0; e < 4; ++e) acc[r][mt][e] += v[r][mt][e][i];
+                }
             }
 #pragma unroll
             for (int r = 0; r < RT; ++r)
