@@ -620,10 +620,10 @@ def run_attn(args):
                                                  ATTENTION_UNITS),
                      "algorithmic_bytes": nbytes, "flops": attention_flops(case),
                      "tflops": attention_flops(case) / per_call / 1e12,
-                     "kernel": "verify_attn_partial_kernel + verify_attn_combine_kernel "
-                               "(time per call, both launches)",
+                     "kernel": "verify_attn_rope_kernel + verify_attn_partial_kernel + "
+                               "verify_attn_combine_kernel (time per call, all three launches)",
                      "us_per_launch": per_call * 1e6},
-        "gpu_launches": 2 * K_steps, "clocks": clk,
+        "gpu_launches": 3 * K_steps, "clocks": clk,
     }
     if rank == 0 and not args.no_cpu:
         import oracle

@@ -360,8 +360,9 @@ int verify_round_multi(const void* h, int B, int L, int K, int N, const uint32_t
  * Sizes         B >= 1, 1 <= L <= 64, Hq a multiple of Hkv, D 64 or 128
  *               (VQ_EUNSUPPORTED otherwise), L <= S_cap <= 2^24, rotary_dim
  *               even in 0..D, theta > 0 when rotary_dim > 0.
- * Two kernels: one per (chunk of 128 keys, KV head, group of 64 query rows,
- * batch row), then one that merges the chunks.
+ * Three kernels: one rotating the block's queries into the workspace and its
+ * keys into the cache (and appending its values), one per (chunk of 64 keys,
+ * KV head, group of 64 query rows, batch row), and one that merges the chunks.
  */
 size_t verify_attention_workspace_bytes(int B, int L, int Hq, int Hkv, int D, int S_cap);
 int verify_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,

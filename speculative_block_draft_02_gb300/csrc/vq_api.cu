@@ -453,6 +453,7 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
 }  // namespace
 
 int num_sms_current_device(int* out) { return device_state(out, nullptr); }
+int device_error_word(int32_t** out) { return device_state(nullptr, out); }
 
 }  // namespace vq
 

@@ -6,24 +6,28 @@
 // own logical positions, and no query sees the stale gap between its row's
 // valid prefix and the verify slots the rectangular cache shares across rows.
 //
-// Two kernels per call:
-//   verify_attn_partial_kernel  one block per (key chunk of 128, KV head, group
+// Three kernels per call:
+//   verify_attn_rope_kernel  one block per (block position j, batch row): the
+//       (cos, sin) of the row's logical position P + j once, then the position's
+//       queries rotated and rounded to the storage type into the workspace, its
+//       keys rotated into cache slot S + j and its values copied to slot S + j.
+//   verify_attn_partial_kernel  one block per (key chunk of 64, KV head, group
 //       of 64 query rows, batch row). It stages the group's rotated queries and
-//       the chunk's keys (prefix slots read from the cache; the block's own keys
-//       rotated at their logical positions, rounded to the storage type and
-//       appended to the cache) and values in shared memory, then four warps of
-//       16 query rows each run S = Q K^T and O += P V on mma.sync m16n8k16 with
-//       an online softmax in fp32. P is split into a 16-bit high part and a
-//       16-bit remainder so that the probabilities keep about 16 significant
-//       bits through the tensor cores. It writes the chunk's unnormalised
-//       output and its (max, sum) per row to the workspace.
+//       the chunk's keys and values (prefix slots, then the block's slots) in
+//       shared memory, every load requested before any is waited for, then four
+//       warps of 16 query rows each run S = Q K^T and O = P V on mma.sync
+//       m16n8k16 with the softmax in fp32. For bf16, P is split into a 16-bit
+//       high part and a 16-bit remainder so that the probabilities keep about
+//       16 significant bits through the tensor cores. It writes the chunk's
+//       unnormalised output and its (max, sum) per row to the workspace.
 //   verify_attn_combine_kernel  merges the chunks of every query row and writes
 //       the 16-bit output.
-// The chunks are small (at most 64 KB of K and V per block) and every block
-// reads its own slice once, so the staging is 16-byte pieces, all requested
-// before any is waited for: cp.async for the query rows and keys, register
-// loads for the values (transposed into shared memory). The merge is launched
-// with programmatic stream serialization and waits for the partial kernel.
+// 52 KB of shared memory and at most 128 registers a thread let four partial
+// blocks share an SM. The partial and the merge kernels are launched with
+// programmatic stream serialization: each may be scheduled while the kernel
+// before it runs and waits for it (griddepcontrol.wait) before reading what it
+// wrote; the partial kernel requests the prefix keys and values, which the
+// rotation kernel does not write, before that wait.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -36,14 +40,14 @@ namespace {
 
 constexpr int kAttnThreads = 128;  // four warps of 16 query rows
 constexpr int kAttnRows = 64;      // query rows per block
-constexpr int kChunk = 128;        // keys per block (one per thread when staging V)
-constexpr int kSub = 64;           // keys per softmax step
+constexpr int kChunk = 64;         // keys per block (two threads per key when staging V)
 constexpr int kMaxRotPairs = 64;   // rotary_dim / 2 for D <= 128
 constexpr int kMaxBlock = 64;      // largest verify block L
 constexpr int kMaxCap = 1 << 24;   // positions stay exact in fp32
 
-static_assert(kChunk == kAttnThreads, "the value tile is staged one key per thread");
-static_assert(kChunk % kSub == 0 && kSub % 16 == 0, "softmax steps cover whole mma k-steps");
+constexpr int kRopeThreads = 256;
+static_assert(kAttnThreads == 2 * kChunk, "the value tile is staged two threads per key");
+static_assert(kChunk == 8 * 8, "the score tile is eight mma n-tiles of 8 keys");
 
 struct AttnParams {
   const uint16_t* q;
@@ -55,8 +59,10 @@ struct AttnParams {
   const int32_t* src_off;
   uint16_t* out;
   int32_t* status;
+  int32_t* err;     // the library's status word (a wait that gave up)
   float* part_o;    // [B][Hkv][RG][NC][64][D]   unnormalised chunk outputs
   float2* part_ml;  // [B][Hkv][RG][NC][64]      (max in log2 units, sum)
+  uint16_t* q_rot;  // [B][L][Hq][D]              rotated, rounded queries
   int L, Hq, Hkv, G, R, RG, NC, S_cap, rot_half;
   float scale_log2;                  // scale * log2(e)
   float2 inv_freq[kMaxRotPairs];     // (hi, lo): hi + lo = theta^(-2i / rotary_dim)
@@ -89,46 +95,102 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
   lo = (uint32_t)f2h<kF16>(a - h2f<kF16>(ha)) | ((uint32_t)f2h<kF16>(b - h2f<kF16>(hb)) << 16);
 }
 
-// 16 bytes global -> shared without a register round trip; zeros when !valid
-// (nothing is read then).
-__device__ __forceinline__ void cp_async_16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_u32(const uint16_t* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
-}
-
 __device__ __forceinline__ bool row_in_range(int P, int S, int L, int S_cap) {
   return P >= 0 && S >= P && (long long)S + L <= (long long)S_cap;
 }
 
-// Turns the pair (x[e], x[e + h]) of a 16-bit row in shared memory by the angle
-// whose (cos, sin) is cs, rounding the results to the storage type.
-template <bool kF16>
-__device__ __forceinline__ void rotate_pair(uint16_t* row, int e, int h, float2 cs) {
-  const float x1 = h2f<kF16>(row[e]), x2 = h2f<kF16>(row[e + h]);
-  row[e] = f2h<kF16>(x1 * cs.x - x2 * cs.y);
-  row[e + h] = f2h<kF16>(x2 * cs.x + x1 * cs.y);
+// (cos, sin) of pos * f for f = hi + lo: the angle is formed as a + err with
+// a = fl(pos * hi) and err the rest of pos * (hi + lo), then turned to first
+// order: sin(a + err) ~ sin a + err cos a (|err| < 1e-3 rad).
+__device__ __forceinline__ float2 rope_cos_sin(float pos, float2 f) {
+  const float a = pos * f.x;
+  const float err = fmaf(pos, f.x, -a) + pos * f.y;
+  float s, c;
+  sincosf(a, &s, &c);
+  return make_float2(c - err * s, s + err * c);
+}
+
+// One block per (block position j, batch row). Rows of the position: the Hq
+// query heads (rotated into the workspace), the Hkv key heads (rotated into
+// cache slot S + j) and the Hkv value heads (copied to slot S + j); dimensions
+// past rotary_dim are copied unchanged. Up to 64 rows at a time go through
+// shared memory: all of their 16-byte loads are requested together, the
+// pairs are turned in place, then the rows are stored in 16-byte pieces.
+template <bool kF16, int D>
+__global__ void __launch_bounds__(kRopeThreads)
+    verify_attn_rope_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int RP = 64;       // rows per pass
+  constexpr int DC = D / 8;    // 16-byte pieces per row
+  __shared__ float2 cs[kMaxRotPairs];
+  __shared__ __align__(16) uint16_t tile[RP * D];
+  grid_launch_dependents();    // the partial kernel may be scheduled; it waits for this one
+  const int j = blockIdx.x, b = blockIdx.y;
+  const int P = p.prefix_len[b], S = p.src_off[b];
+  if (!row_in_range(P, S, p.L, p.S_cap)) return;   // flagged by the combine kernel
+  const int rh = p.rot_half;
+  const int tid = threadIdx.x;
+  // row r of the position: where it comes from and where it goes
+  auto row_src = [&](int r) -> const uint16_t* {
+    if (r < p.Hq) return p.q + (((size_t)b * p.L + j) * p.Hq + r) * D;
+    if (r < p.Hq + p.Hkv) return p.k_new + (((size_t)b * p.L + j) * p.Hkv + (r - p.Hq)) * D;
+    return p.v_new + (((size_t)b * p.L + j) * p.Hkv + (r - p.Hq - p.Hkv)) * D;
+  };
+  auto row_dst = [&](int r) -> uint16_t* {
+    if (r < p.Hq) return p.q_rot + (((size_t)b * p.L + j) * p.Hq + r) * D;
+    const int h = r < p.Hq + p.Hkv ? r - p.Hq : r - p.Hq - p.Hkv;
+    uint16_t* cache = r < p.Hq + p.Hkv ? p.k_cache : p.v_cache;
+    return cache + (((size_t)b * p.Hkv + h) * p.S_cap + (S + j)) * D;
+  };
+  const int rows = p.Hq + 2 * p.Hkv, n_rot = p.Hq + p.Hkv;
+  for (int r0 = 0; r0 < rows; r0 += RP) {
+    const int nr = min(RP, rows - r0);
+    if (r0 > 0) __syncthreads();   // the previous pass has stored its rows
+#pragma unroll 4
+    for (int i = tid; i < nr * DC; i += kRopeThreads) {
+      const int rl = i / DC, c = i - rl * DC;
+      *reinterpret_cast<uint4*>(tile + rl * D + c * 8) =
+          __ldg(reinterpret_cast<const uint4*>(row_src(r0 + rl)) + c);
+    }
+    // the angles of the position, while the first rows are in flight
+    if (r0 == 0)
+      for (int e = tid; e < rh; e += kRopeThreads) cs[e] = rope_cos_sin((float)(P + j), p.inv_freq[e]);
+    __syncthreads();
+    const int nrot = max(0, min(nr, n_rot - r0));   // rows of this pass that turn
+    for (int i = tid; i < nrot * rh; i += kRopeThreads) {
+      const int rl = i / rh, e = i - rl * rh;
+      uint16_t* row = tile + rl * D;
+      const float x1 = h2f<kF16>(row[e]), x2 = h2f<kF16>(row[e + rh]);
+      row[e] = f2h<kF16>(x1 * cs[e].x - x2 * cs[e].y);
+      row[e + rh] = f2h<kF16>(x2 * cs[e].x + x1 * cs[e].y);
+    }
+    __syncthreads();
+    for (int i = tid; i < nr * DC; i += kRopeThreads) {
+      const int rl = i / DC, c = i - rl * DC;
+      reinterpret_cast<uint4*>(row_dst(r0 + rl))[c] =
+          *reinterpret_cast<const uint4*>(tile + rl * D + c * 8);
+    }
+  }
+}
+
+// A bounded wait on phase 0 of an mbarrier: false after about a second.
+__device__ __forceinline__ bool attn_wait(uint32_t bar) {
+  if (mbar_try_wait(bar, 0u)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, 0u))
+    if (clock64() - t0 > kWaitTimeoutCycles) return false;
+  return true;
 }
 
 template <bool kF16, int D>
-__global__ void __launch_bounds__(kAttnThreads)
+__global__ void __launch_bounds__(kAttnThreads, 4)
     verify_attn_partial_kernel(const __grid_constant__ AttnParams p) {
-  constexpr int QS = D + 8;        // row stride of the query and key tiles (16-bit elements)
-  constexpr int VS = kChunk + 8;   // row stride of the transposed value tile
-  constexpr int DC = D / 8;        // 16-byte pieces per row
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);   // [64][QS]
-  uint16_t* Ks = Qs + kAttnRows * QS;                  // [kChunk][QS]
-  uint16_t* Vt = Ks + kChunk * QS;                     // [D][VS]: Vt[d][key]
-  float2* cs = reinterpret_cast<float2*>(Vt + D * VS); // [L][rot_half] (cos, sin)
+  constexpr int QS = D + 8;               // row stride of the tiles (16-bit elements)
+  constexpr uint32_t RB = D * 2;          // bytes of one row
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);   // [64][QS] rotated queries
+  uint16_t* Ks = Qs + kAttnRows * QS;                  // [64][QS] keys
+  uint16_t* Vs = Ks + kChunk * QS;                     // [64][QS] values
+  const uint32_t bar_pre = smem_addr(Vs + kChunk * QS), bar_rest = bar_pre + 8u;
 
   const int chunk = blockIdx.x;
   const int hk = blockIdx.y / p.RG, rg = blockIdx.y % p.RG;
@@ -139,105 +201,68 @@ __global__ void __launch_bounds__(kAttnThreads)
   const int c0 = chunk * kChunk;
   if (c0 >= T) return;
   const int tid = threadIdx.x;
-  const int rh = p.rot_half;
-  grid_launch_dependents();
+  grid_launch_dependents();   // the merge may be scheduled; it waits for this kernel
+  if (tid == 0) {
+    mbar_init(bar_pre, 1);
+    mbar_init(bar_rest, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
 
-  // Every load of the stage is issued before any of them is waited for: the
-  // query rows and the keys go global -> shared asynchronously, the values
-  // (transposed on the way) through registers.
-  // Query rows of this group: row r = j * G + (hq - hk * G).
-  for (int i = tid; i < kAttnRows * DC; i += kAttnThreads) {
-    const int r = i / DC, dc = i - r * DC;
-    const int rr = rg * kAttnRows + r;
-    const uint16_t* src = p.q;
-    if (rr < p.R) {
+  // Key tl of the chunk (t = c0 + tl) sits in cache slot t below P and in slot
+  // S + (t - P) from P on. Rows arrive by bulk copies, one per row: the prefix
+  // rows are requested before the wait for the rotation kernel (which writes
+  // only slots S.. and the rotated queries; everything before it in the stream
+  // had completed when it started), the queries and the block's rows after it.
+  const size_t head = ((size_t)b * p.Hkv + hk) * p.S_cap;
+  const int n_pre = max(0, min(P - c0, kChunk));   // prefix keys: tl < n_pre
+  const int n_vis = min(T - c0, kChunk);           // visible keys: tl < n_vis
+  const int nq = min(kAttnRows, p.R - rg * kAttnRows);
+  if (tid < 32) {
+    if (tid == 0) mbar_arrive_expect_tx(bar_pre, 2u * (uint32_t)n_pre * RB);
+    __syncwarp();
+    for (int tl = tid; tl < n_pre; tl += 32) {
+      const size_t slot = head + (size_t)(c0 + tl);
+      bulk_load(smem_addr(Ks + tl * QS), p.k_cache + slot * D, RB, bar_pre);
+      bulk_load(smem_addr(Vs + tl * QS), p.v_cache + slot * D, RB, bar_pre);
+    }
+  }
+  grid_wait_prerequisites();
+  if (tid < 32) {
+    if (tid == 0) mbar_arrive_expect_tx(bar_rest, (uint32_t)(2 * (n_vis - n_pre) + nq) * RB);
+    __syncwarp();
+    for (int tl = n_pre + tid; tl < n_vis; tl += 32) {
+      const size_t slot = head + (size_t)(S + (c0 + tl - P));
+      bulk_load(smem_addr(Ks + tl * QS), p.k_cache + slot * D, RB, bar_rest);
+      bulk_load(smem_addr(Vs + tl * QS), p.v_cache + slot * D, RB, bar_rest);
+    }
+    // query row r = j * G + (hq - hk * G) of the group
+    for (int r = tid; r < nq; r += 32) {
+      const int rr = rg * kAttnRows + r;
       const int j = rr / p.G, hq = hk * p.G + (rr - j * p.G);
-      src = p.q + (((size_t)b * p.L + j) * p.Hq + hq) * D + dc * 8;
-    }
-    cp_async_16(Qs + r * QS + dc * 8, src, rr < p.R);
-  }
-  // Keys: prefix slots from the cache, the block's keys (rotated below), zeros past T.
-  for (int i = tid; i < kChunk * DC; i += kAttnThreads) {
-    const int tl = i / DC, dc = i - tl * DC;
-    const int t = c0 + tl;
-    const uint16_t* src = p.k_cache;
-    if (t < P) {
-      src = p.k_cache + (((size_t)b * p.Hkv + hk) * p.S_cap + t) * D + dc * 8;
-    } else if (t < T) {
-      src = p.k_new + (((size_t)b * p.L + (t - P)) * p.Hkv + hk) * D + dc * 8;
-    }
-    cp_async_16(Ks + tl * QS + dc * 8, src, t < T);
-  }
-  // Values: thread tid owns key c0 + tid.
-  uint4 vv[DC];
-  {
-    const int t = c0 + tid;
-    const uint16_t* src = nullptr;
-    if (t < P) {
-      src = p.v_cache + (((size_t)b * p.Hkv + hk) * p.S_cap + t) * D;
-    } else if (t < T) {
-      src = p.v_new + (((size_t)b * p.L + (t - P)) * p.Hkv + hk) * D;
-    }
-#pragma unroll
-    for (int dc = 0; dc < DC; ++dc)
-      vv[dc] = src ? __ldg(reinterpret_cast<const uint4*>(src) + dc) : make_uint4(0u, 0u, 0u, 0u);
-  }
-
-  // (cos, sin) of every block position's angles, while the loads are in flight.
-  // The angle pos * f is formed as a + err with a = fl(pos * hi) and err the rest
-  // of pos * (hi + lo), then turned to first order: sin(a + err) ~ sin a + err cos a
-  // (|err| < 1e-3 rad).
-  for (int i = tid; i < p.L * rh; i += kAttnThreads) {
-    const int j = i / rh, e = i - j * rh;
-    const float pos = (float)(P + j);
-    const float2 f = p.inv_freq[e];
-    const float a = pos * f.x;
-    const float err = fmaf(pos, f.x, -a) + pos * f.y;
-    float s, c;
-    sincosf(a, &s, &c);
-    cs[i] = make_float2(c - err * s, s + err * c);
-  }
-
-#pragma unroll
-  for (int dc = 0; dc < DC; ++dc) {
-    const uint32_t w[4] = {vv[dc].x, vv[dc].y, vv[dc].z, vv[dc].w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      Vt[(dc * 8 + 2 * e) * VS + tid] = (uint16_t)(w[e] & 0xFFFFu);
-      Vt[(dc * 8 + 2 * e + 1) * VS + tid] = (uint16_t)(w[e] >> 16);
+      bulk_load(smem_addr(Qs + r * QS), p.q_rot + (((size_t)b * p.L + j) * p.Hq + hq) * D, RB,
+                bar_rest);
     }
   }
-  cp_async_wait_all();
-  __syncthreads();
-
-  // Rotate the queries and the block's keys at their logical positions P + j.
-  for (int i = tid; i < kAttnRows * rh; i += kAttnThreads) {
-    const int r = i / rh, e = i - r * rh;
-    const int rr = rg * kAttnRows + r;
-    if (rr < p.R) rotate_pair<kF16>(Qs + r * QS, e, rh, cs[(rr / p.G) * rh + e]);
+  // rows no copy fills: keys past the last visible one (their values must be
+  // finite, as their probabilities are 0) and query rows past the group's
+  for (int i = tid; i < (kChunk - n_vis) * (D / 8); i += kAttnThreads) {
+    const int tl = n_vis + i / (D / 8), c = i % (D / 8);
+    *reinterpret_cast<uint4*>(Ks + tl * QS + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(Vs + tl * QS + c * 8) = make_uint4(0u, 0u, 0u, 0u);
   }
-  const int tb0 = max(c0, P) - c0;               // first block key in this chunk
-  const int nb = min(c0 + kChunk, T) - c0 - tb0;  // block keys in this chunk (may be <= 0)
-  for (int i = tid; i < max(nb, 0) * rh; i += kAttnThreads) {
-    const int k = i / rh, e = i - k * rh;
-    const int tl = tb0 + k;
-    rotate_pair<kF16>(Ks + tl * QS, e, rh, cs[(c0 + tl - P) * rh + e]);
+  for (int i = tid; i < (kAttnRows - nq) * (D / 8); i += kAttnThreads) {
+    const int r = nq + i / (D / 8), c = i % (D / 8);
+    *reinterpret_cast<uint4*>(Qs + r * QS + c * 8) = make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
-
-  // Append the block's keys and values at slots S + j (one row group writes).
-  if (rg == 0) {
-    for (int i = tid; i < max(nb, 0) * DC; i += kAttnThreads) {
-      const int k = i / DC, dc = i - k * DC;
-      const int tl = tb0 + k;
-      const int j = c0 + tl - P;
-      const size_t slot = (((size_t)b * p.Hkv + hk) * p.S_cap + (S + j)) * D;
-      reinterpret_cast<uint4*>(p.k_cache + slot)[dc] =
-          *reinterpret_cast<const uint4*>(Ks + tl * QS + dc * 8);
-      reinterpret_cast<uint4*>(p.v_cache + slot)[dc] = __ldg(
-          reinterpret_cast<const uint4*>(p.v_new + (((size_t)b * p.L + j) * p.Hkv + hk) * D) + dc);
-    }
+  if (!attn_wait(bar_pre) || !attn_wait(bar_rest)) {
+    // give up: report it, let the copies already issued land, and leave
+    if (tid == 0) atomicOr(p.err, kErrWaitTimeout);
+    attn_wait(bar_pre);
+    attn_wait(bar_rest);
+    return;
   }
+  __syncthreads();   // the zero rows too
 
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
   const int row0 = warp * 16;
@@ -246,89 +271,97 @@ __global__ void __launch_bounds__(kAttnThreads)
   const bool okA = rA < p.R, okB = rB < p.R;
   const int jA = rA / p.G, jB = rB / p.G;
 
-  uint32_t qa[D / 16][4];
+  // S = Q K^T: A fragments of the warp's 16 query rows, B fragments of two
+  // 8-key tiles per ldmatrix.x4
+  float sc[8][4];
+#pragma unroll
+  for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  const uint32_t qa_addr = smem_addr(Qs + (row0 + (lane & 15)) * QS + (lane >> 4) * 8);
+  const uint32_t kb_addr =
+      smem_addr(Ks + ((lane & 7) + ((lane >> 4) << 3)) * QS + ((lane >> 3) & 1) * 8);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    const uint16_t* q0 = Qs + (row0 + g) * QS + ks * 16 + 2 * tq;
-    qa[ks][0] = ld_u32(q0);
-    qa[ks][1] = ld_u32(q0 + 8 * QS);
-    qa[ks][2] = ld_u32(q0 + 8);
-    qa[ks][3] = ld_u32(q0 + 8 * QS + 8);
-  }
-  float o[D / 8][4];
+    uint32_t qa[4];
+    ldsm_x4(qa, qa_addr + ks * 32);
 #pragma unroll
-  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-
-#pragma unroll 1
-  for (int st = 0; st < kChunk / kSub; ++st) {
-    const int kb = c0 + st * kSub;
-    if (kb >= T) break;
-    float sc[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const uint16_t* k0 = Ks + (st * kSub + nt * 8 + g) * QS + ks * 16 + 2 * tq;
-        mma_16816<kF16>(sc[nt], qa[ks], ld_u32(k0), ld_u32(k0 + 8));
-      }
+    for (int np = 0; np < 4; ++np) {
+      uint32_t kb[4];
+      ldsm_x4(kb, kb_addr + (np * 16 * QS + ks * 16) * 2);
+      mma_16816<kF16>(sc[2 * np], qa, kb[0], kb[1]);
+      mma_16816<kF16>(sc[2 * np + 1], qa, kb[2], kb[3]);
     }
-    // mask (prefix for all, block keys causally, nothing past T), scale, row max
-    float mx[2] = {-INFINITY, -INFINITY};
+  }
+  // mask (prefix for all, block keys causally, nothing past T), scale, row max;
+  // a chunk wholly in the prefix is visible to every row
+  float m[2] = {-INFINITY, -INFINITY};
+  if (c0 + kChunk <= P) {
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        sc[nt][e] *= p.scale_log2;
+        m[e >> 1] = fmaxf(m[e >> 1], sc[nt][e]);
+      }
+  } else {
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int t = kb + nt * 8 + 2 * tq + (e & 1);
+        const int t = c0 + nt * 8 + 2 * tq + (e & 1);
         const int hh = e >> 1;
         const bool vis = (hh ? okB : okA) && t < T && (t < P || t - P <= (hh ? jB : jA));
         const float v = vis ? sc[nt][e] * p.scale_log2 : -INFINITY;
         sc[nt][e] = v;
-        mx[hh] = fmaxf(mx[hh], v);
-      }
-    }
-    float mu[2];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 1));
-      mx[hh] = fmaxf(mx[hh], __shfl_xor_sync(0xffffffffu, mx[hh], 2));
-      const float mn = fmaxf(m[hh], mx[hh]);
-      mu[hh] = mn == -INFINITY ? 0.f : mn;        // no visible key yet: nothing to scale
-      const float alpha = exp2f(m[hh] - mu[hh]);
-      m[hh] = mn;
-      l[hh] *= alpha;
-#pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        o[nd][2 * hh] *= alpha;
-        o[nd][2 * hh + 1] *= alpha;
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < kSub / 16; ++kk) {
-      uint32_t ah[4], al[4];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int nt = 2 * kk + half;
-        const float p0 = exp2f(sc[nt][0] - mu[0]), p1 = exp2f(sc[nt][1] - mu[0]);
-        const float p2 = exp2f(sc[nt][2] - mu[1]), p3 = exp2f(sc[nt][3] - mu[1]);
-        l[0] += p0 + p1;
-        l[1] += p2 + p3;
-        split_pair<kF16>(p0, p1, ah[2 * half], al[2 * half]);
-        split_pair<kF16>(p2, p3, ah[2 * half + 1], al[2 * half + 1]);
-      }
-#pragma unroll
-      for (int nd = 0; nd < D / 8; ++nd) {
-        const uint16_t* v0 = Vt + (nd * 8 + g) * VS + st * kSub + kk * 16 + 2 * tq;
-        const uint32_t b0 = ld_u32(v0), b1 = ld_u32(v0 + 8);
-        mma_16816<kF16>(o[nd], ah, b0, b1);
-        mma_16816<kF16>(o[nd], al, b0, b1);
+        m[hh] = fmaxf(m[hh], v);
       }
     }
   }
-
+  float mu[2], l[2] = {0.f, 0.f};
 #pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    m[hh] = fmaxf(m[hh], __shfl_xor_sync(0xffffffffu, m[hh], 1));
+    m[hh] = fmaxf(m[hh], __shfl_xor_sync(0xffffffffu, m[hh], 2));
+    mu[hh] = m[hh] == -INFINITY ? 0.f : m[hh];   // no visible key in the chunk: every p is 0
+  }
+  float o[D / 8][4];
+#pragma unroll
+  for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  // O = P V: P as 16-bit MMA operands. bf16 keeps 8 significant bits, which
+  // would move the outputs by up to 2^-9 relative, so there P is split into a
+  // high part and the remainder (two MMAs, about 16 bits); fp16's 11 bits
+  // suffice alone. B fragments of two 8-dimension tiles per ldmatrix.x4.trans.
+  const uint32_t vb_addr =
+      smem_addr(Vs + ((lane & 7) + ((lane >> 3) & 1) * 8) * QS + (lane >> 4) * 8);
+#pragma unroll
+  for (int kk = 0; kk < kChunk / 16; ++kk) {
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int nt = 2 * kk + half;
+      const float p0 = exp2f(sc[nt][0] - mu[0]), p1 = exp2f(sc[nt][1] - mu[0]);
+      const float p2 = exp2f(sc[nt][2] - mu[1]), p3 = exp2f(sc[nt][3] - mu[1]);
+      l[0] += p0 + p1;
+      l[1] += p2 + p3;
+      if constexpr (kF16) {
+        ah[2 * half] = (uint32_t)f2h<true>(p0) | ((uint32_t)f2h<true>(p1) << 16);
+        ah[2 * half + 1] = (uint32_t)f2h<true>(p2) | ((uint32_t)f2h<true>(p3) << 16);
+      } else {
+        split_pair<false>(p0, p1, ah[2 * half], al[2 * half]);
+        split_pair<false>(p2, p3, ah[2 * half + 1], al[2 * half + 1]);
+      }
+    }
+#pragma unroll
+    for (int np = 0; np < D / 16; ++np) {
+      uint32_t vb[4];
+      ldsm_x4_t(vb, vb_addr + (kk * 16 * QS + np * 16) * 2);
+      mma_16816<kF16>(o[2 * np], ah, vb[0], vb[1]);
+      mma_16816<kF16>(o[2 * np + 1], ah, vb[2], vb[3]);
+      if constexpr (!kF16) {
+        mma_16816<kF16>(o[2 * np], al, vb[0], vb[1]);
+        mma_16816<kF16>(o[2 * np + 1], al, vb[2], vb[3]);
+      }
+    }
+  }
   for (int hh = 0; hh < 2; ++hh) {
     l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 1);
     l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 2);
@@ -351,35 +384,80 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
 }
 
-// One block per (block position j, query head), one thread per dimension.
+// One block per (block position j, query head, batch row), D threads. Lane l of
+// every warp covers dimensions VEC*l .. VEC*l + VEC-1; warp w takes chunks w,
+// w + NW, ... so that all of a row's chunks are requested at once; the warps'
+// sums are then added in warp order (a fixed order: the result does not depend
+// on timing).
 template <bool kF16, int D>
 __global__ void __launch_bounds__(D) verify_attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int NW = D / 32, VEC = D / 32;
   const int jh = blockIdx.x, b = blockIdx.y;
   const int j = jh / p.Hq, hq = jh - j * p.Hq;
-  const int d = threadIdx.x;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   grid_wait_prerequisites();   // launched early (programmatic serialization)
   uint16_t* dst = p.out + (((size_t)b * p.L + j) * p.Hq + hq) * D;
   const int P = p.prefix_len[b], S = p.src_off[b];
   if (!row_in_range(P, S, p.L, p.S_cap)) {
-    dst[d] = 0;
-    if (jh == 0 && d == 0 && p.status) atomicOr(p.status, 1);
+    dst[tid] = 0;
+    if (jh == 0 && tid == 0 && p.status) atomicOr(p.status, 1);
     return;
   }
   const int nc = (P + p.L + kChunk - 1) / kChunk;
   const int hk = hq / p.G, rr = j * p.G + (hq - hk * p.G);
   const int rg = rr / kAttnRows, lr = rr - rg * kAttnRows;
   const size_t part0 = (((size_t)b * p.Hkv + hk) * p.RG + rg) * p.NC;
-  // every query sees its own key, so some chunk has a finite maximum
-  float mmax = -INFINITY;
-  for (int c = 0; c < nc; ++c) mmax = fmaxf(mmax, p.part_ml[(part0 + c) * kAttnRows + lr].x);
-  float acc = 0.f, den = 0.f;
-  for (int c = 0; c < nc; ++c) {
-    const float2 ml = p.part_ml[(part0 + c) * kAttnRows + lr];
-    const float w = exp2f(ml.x - mmax);
-    den += w * ml.y;
-    acc += w * p.part_o[((part0 + c) * kAttnRows + lr) * D + d];
+  const float2* ml = p.part_ml + part0 * kAttnRows + lr;                    // chunk c at ml[c * 64]
+  const float* po = p.part_o + (part0 * kAttnRows + lr) * D + VEC * lane;   // at po[c * 64 * D]
+  // the chunks' maxima: strided over the threads, then over the block; every
+  // query sees its own key, so some chunk has a finite maximum
+  __shared__ float red_m[NW];
+  __shared__ float red_s[NW][VEC * 32 + 1];   // each warp's sums, then its denominator
+  float mx = -INFINITY;
+  for (int c = tid; c < nc; c += D) mx = fmaxf(mx, ml[(size_t)c * kAttnRows].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red_m[w] = mx;
+  __syncthreads();
+  float mmax = red_m[0];
+#pragma unroll
+  for (int i = 1; i < NW; ++i) mmax = fmaxf(mmax, red_m[i]);
+  float acc[VEC], den = 0.f;
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+#pragma unroll 4
+  for (int c = w; c < nc; c += NW) {
+    const float2 mc = ml[(size_t)c * kAttnRows];
+    const float* src = po + (size_t)c * kAttnRows * D;
+    float x[VEC];
+    if constexpr (VEC == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(src);
+      x[0] = t.x;
+      x[1] = t.y;
+      x[2] = t.z;
+      x[3] = t.w;
+    } else {
+      const float2 t = *reinterpret_cast<const float2*>(src);
+      x[0] = t.x;
+      x[1] = t.y;
+    }
+    const float wt = exp2f(mc.x - mmax);
+    den += wt * mc.y;
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] += wt * x[v];
   }
-  dst[d] = f2h<kF16>(acc / den);
+#pragma unroll
+  for (int v = 0; v < VEC; ++v) red_s[w][VEC * lane + v] = acc[v];
+  if (lane == 0) red_s[w][VEC * 32] = den;
+  __syncthreads();
+  // thread tid writes dimension tid: the warps' sums in warp order
+  float o = red_s[0][tid], dsum = red_s[0][VEC * 32];
+#pragma unroll
+  for (int i = 1; i < NW; ++i) {
+    o += red_s[i][tid];
+    dsum += red_s[i][VEC * 32];
+  }
+  dst[tid] = f2h<kF16>(o / dsum);
 }
 
 int attn_check(const void* q, const void* k_new, const void* v_new, const void* k_cache,
@@ -425,14 +503,34 @@ size_t attn_part_count(int B, int Hkv, const AttnShape& s) {
   return (size_t)B * Hkv * s.RG * s.NC * kAttnRows;
 }
 
+// Byte offset of the rotated queries in the workspace (rows: partial-result rows).
+size_t attn_qrot_offset(size_t rows, int D) {
+  return (rows * (size_t)D * sizeof(float) + rows * sizeof(float2) + 15) / 16 * 16;
+}
+
 template <bool kF16, int D>
 int attn_launch(const AttnParams& p, int B, cudaStream_t stream) {
-  const size_t smem = (size_t)(kAttnRows + kChunk) * (D + 8) * 2 + (size_t)D * (kChunk + 8) * 2 +
-                      (size_t)p.L * p.rot_half * sizeof(float2);
+  // the three tiles and two mbarriers
+  const size_t smem = (size_t)(kAttnRows + 2 * kChunk) * (D + 8) * 2 + 16;
   auto* partial = verify_attn_partial_kernel<kF16, D>;
   if (ensure_smem<verify_attn_partial_kernel<kF16, D>>(smem) != VQ_OK) return VQ_ECUDA;
-  partial<<<dim3(p.NC, p.Hkv * p.RG, B), kAttnThreads, smem, stream>>>(p);
+  // the rotation runs after everything before it in the stream; the partial
+  // kernel may be scheduled while it runs and waits for it on the GPU
+  verify_attn_rope_kernel<kF16, D><<<dim3(p.L, B), kRopeThreads, 0, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return VQ_ECUDA;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.NC, p.Hkv * p.RG, B);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, partial, p) != cudaSuccess) return VQ_ECUDA;
+  }
   // the merge may be scheduled while the partial kernel runs; it waits for it
   // (griddepcontrol.wait) before reading anything
   cudaLaunchConfig_t cfg = {};
@@ -460,7 +558,8 @@ extern "C" size_t verify_attention_workspace_bytes(int B, int L, int Hq, int Hkv
   if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || S_cap < 1) return 0;
   const AttnShape s = attn_shape(L, Hq, Hkv, S_cap);
   const size_t rows = attn_part_count(B, Hkv, s);
-  return rows * (size_t)D * sizeof(float) + rows * sizeof(float2);
+  // [partial outputs][partial (max, sum)][rotated queries], each 16-byte aligned
+  return attn_qrot_offset(rows, D) + (size_t)B * L * Hq * D * sizeof(uint16_t);
 }
 
 extern "C" int verify_attention(const void* q, const void* k_new, const void* v_new,
@@ -474,7 +573,8 @@ extern "C" int verify_attention(const void* q, const void* k_new, const void* v_
   if (rc) return rc;
   const size_t need = verify_attention_workspace_bytes(B, L, Hq, Hkv, D, S_cap);
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 15u)) return VQ_EWORKSPACE;
-  rc = num_sms_current_device(nullptr);   // a usable current device
+  int32_t* err = nullptr;   // the device's status word (a usable current device)
+  rc = device_error_word(&err);
   if (rc) return rc;
 
   const AttnShape s = attn_shape(L, Hq, Hkv, S_cap);
@@ -488,10 +588,12 @@ extern "C" int verify_attention(const void* q, const void* k_new, const void* v_
   p.src_off = src_off;
   p.out = static_cast<uint16_t*>(out);
   p.status = status;
+  p.err = err;
   const size_t rows = attn_part_count(B, Hkv, s);
   p.part_o = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
                                         rows * (size_t)D * sizeof(float));
+  p.q_rot = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + attn_qrot_offset(rows, D));
   p.L = L;
   p.Hq = Hq;
   p.Hkv = Hkv;

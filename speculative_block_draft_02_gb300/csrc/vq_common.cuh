@@ -174,6 +174,20 @@ __device__ __forceinline__ void mma_16816_zc(float (&d)[4], const uint32_t (&a)[
   }
 }
 
+// Four 8x8 tiles of 16-bit values from shared memory: thread i gives the
+// address of row i % 8 of tile i / 8; thread t receives row t / 4, elements
+// 2 (t % 4) and 2 (t % 4) + 1 of every tile (of the transposed tile with .trans).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -230,6 +244,8 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
 
 namespace vq {
 int num_sms_current_device(int* out);
+// The device's status word (kErrWaitTimeout ...) for kernels that report into it.
+int device_error_word(int32_t** out);
 
 // Raises kernel K's dynamic shared-memory limit on the current device to at
 // least `bytes`, calling the runtime only the first time a device needs a
