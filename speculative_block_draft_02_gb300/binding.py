@@ -57,6 +57,8 @@ class VQError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """The loaded CUDA library. Raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -77,13 +79,15 @@ def _check(rc: int, what: str):
 
 
 def _ptr(t):
+    """The device address of a contiguous CUDA tensor as an int (ctypes passes
+    it as the void* of the signature), None for None."""
     if t is None:
         return None
     if not t.is_cuda:
         raise VQError("expected a CUDA tensor")
     if not t.is_contiguous():
         raise VQError("expected a contiguous tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
@@ -94,10 +98,10 @@ def _stream(stream):
     current device (read without building a Stream object, which costs a few
     microseconds per call)."""
     if stream is not None:
-        return ctypes.c_void_p(stream.cuda_stream)
+        return stream.cuda_stream
     if _raw_stream is not None:
-        return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        return _raw_stream(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def vq_linear_workspace_bytes(M: int, K: int, N: int, act=torch.bfloat16) -> int:
@@ -114,7 +118,7 @@ def vq_linear(x, qw, scales, biases, y=None, workspace=None, stream=None):
     N = qw.shape[0]
     if y is None:
         y = torch.empty((M, N), dtype=x.dtype, device=x.device)
-    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ws_bytes = 0 if workspace is None else workspace.nbytes
     rc = lib().vq_linear(_ptr(x), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases), _ptr(y),
                          _ACT[x.dtype], _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "vq_linear")
@@ -129,7 +133,7 @@ def vq_vocab_argmax(x, qw, scales, biases, workspace, argmax=None, maxval=None, 
         argmax = torch.empty(M, dtype=torch.int32, device=x.device)
     rc = lib().vq_vocab_argmax(_ptr(x), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
                                _ACT[x.dtype], _ptr(argmax), _ptr(maxval), _ptr(workspace),
-                               workspace.numel() * workspace.element_size(), _stream(stream))
+                               workspace.nbytes, _stream(stream))
     _check(rc, "vq_vocab_argmax")
     return argmax, maxval
 
@@ -152,7 +156,7 @@ def vq_vocab_argmax_top2(x, qw, scales, biases, workspace, argmax=None, maxval=N
         second = torch.empty(M, dtype=torch.float32, device=x.device)
     rc = lib().vq_vocab_argmax_top2(_ptr(x), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
                                     _ACT[x.dtype], _ptr(argmax), _ptr(maxval), _ptr(second),
-                                    _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _ptr(workspace), workspace.nbytes,
                                     _stream(stream))
     _check(rc, "vq_vocab_argmax_top2")
     return argmax, maxval, second
@@ -183,7 +187,7 @@ def kv_compact_per_row(tensors, prefix_len, src_off, keep, max_keep: int, new_le
                        status=None, stream=None):
     t0 = tensors[0]
     B, H, S_cap, D = t0.shape
-    arr = (ctypes.c_void_p * len(tensors))(*[_ptr(t).value for t in tensors])
+    arr = (ctypes.c_void_p * len(tensors))(*[_ptr(t) for t in tensors])
     if new_len is None:
         new_len = torch.empty(B, dtype=torch.int32, device=t0.device)
     rc = lib().kv_compact_per_row(ctypes.cast(arr, ctypes.c_void_p), len(tensors), B, H, S_cap, D,
@@ -215,7 +219,7 @@ def verify_round(h, qw, scales, biases, tokens, workspace, kv=None, prefix_len=N
     if kv:
         t0 = kv[0]
         _, H, S_cap, D = t0.shape
-        arr = (ctypes.c_void_p * len(kv))(*[_ptr(t).value for t in kv])
+        arr = (ctypes.c_void_p * len(kv))(*[_ptr(t) for t in kv])
         if new_len is None:
             new_len = torch.empty(B, dtype=torch.int32, device=dev)
         kv_args = (ctypes.cast(arr, ctypes.c_void_p), len(kv), H, S_cap, D, t0.element_size(),
@@ -224,7 +228,7 @@ def verify_round(h, qw, scales, biases, tokens, workspace, kv=None, prefix_len=N
         kv_args = (None, 0, 0, 0, 0, 0, None, None, None, None)
     rc = lib().verify_round(_ptr(h), B, L, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
                             _ACT[h.dtype], _ptr(tokens), _ptr(target), _ptr(accept), _ptr(bonus),
-                            *kv_args, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            *kv_args, _ptr(workspace), workspace.nbytes,
                             _stream(stream))
     _check(rc, "verify_round")
     return target, accept, bonus, (new_len if kv else None)
@@ -260,7 +264,7 @@ def verify_round_multi(h, qw, scales, biases, tokens, workspace, sets=(), status
     for i, (kv, prefix_len, src_off) in enumerate(sets):
         t0 = kv[0]
         _, H, S_cap, D = t0.shape
-        arr = (ctypes.c_void_p * len(kv))(*[_ptr(t).value for t in kv])
+        arr = (ctypes.c_void_p * len(kv))(*[_ptr(t) for t in kv])
         keep_alive.append(arr)
         nl = torch.empty(B, dtype=torch.int32, device=dev)
         new_lens.append(nl)
@@ -270,7 +274,7 @@ def verify_round_multi(h, qw, scales, biases, tokens, workspace, sets=(), status
                                   _ACT[h.dtype], _ptr(tokens), _ptr(target), _ptr(accept),
                                   _ptr(bonus), ctypes.cast(descs, ctypes.c_void_p), len(sets),
                                   _ptr(status), _ptr(workspace),
-                                  workspace.numel() * workspace.element_size(), _stream(stream))
+                                  workspace.nbytes, _stream(stream))
     _check(rc, "verify_round_multi")
     return target, accept, bonus, new_lens
 
@@ -309,7 +313,7 @@ def verify_attention(q, k_new, v_new, k_cache, v_cache, prefix_len, src_off, wor
                                 _ptr(prefix_len), _ptr(src_off), _ptr(out), B, L, Hq, Hkv, D,
                                 S_cap, rotary_dim, float(theta), float(scale), _ACT[q.dtype],
                                 _ptr(status), _ptr(workspace),
-                                workspace.numel() * workspace.element_size(),
+                                workspace.nbytes,
                                 _stream(stream))
     _check(rc, "verify_attention")
     return out

@@ -66,3 +66,31 @@ def to_dev_weights(w: synth.W4Weights):
 
 def out_to_f64(y: torch.Tensor) -> np.ndarray:
     return y.float().cpu().numpy().astype(np.float64)
+
+
+# Canary guard regions (a stand-in for a memory checker): an output handed to a
+# kernel is a view into a larger device buffer whose bytes on both sides hold a
+# known pattern; check() fails if any of them changed, i.e. if the kernel wrote
+# outside the tensor it was given.
+GUARD_BYTES = 4096      # on each side; keeps the tensor 256-byte aligned
+_CANARY = 0xA5
+
+
+class Guarded:
+    def __init__(self, shape, dtype, fill=None):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.n = n
+        self.raw = torch.full((n + 2 * GUARD_BYTES,), _CANARY, dtype=torch.uint8, device="cuda")
+        self.t = self.raw[GUARD_BYTES:GUARD_BYTES + n].view(dtype).view(shape)
+        if fill is not None:
+            if isinstance(fill, torch.Tensor):
+                self.t.copy_(fill)
+            else:
+                self.t.fill_(fill)
+
+    def check(self):
+        torch.cuda.synchronize()
+        head = self.raw[:GUARD_BYTES]
+        tail = self.raw[GUARD_BYTES + self.n:]
+        assert bool((head == _CANARY).all()) and bool((tail == _CANARY).all()), \
+            "a kernel wrote outside the %d-byte tensor it was given" % self.n

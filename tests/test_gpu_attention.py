@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from parity import TOL, proj_error
+from parity import TOL, Guarded, proj_error
 from speculative_block_draft_02_gb300 import binding as vq
 from speculative_block_draft_02_gb300 import synth
 
@@ -58,17 +58,21 @@ def run_both(case, rotary_dim, theta, scale=None, ws_fill=0xFF):
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     dt = case.dtype
     q, kn, vn = dev(case.q, dt), dev(case.k_new, dt), dev(case.v_new, dt)
-    kc, vc = dev(case.k_cache, dt), dev(case.v_cache, dt)
+    gk = Guarded(case.k_cache.shape, TDT[dt], fill=dev(case.k_cache, dt))
+    gv = Guarded(case.v_cache.shape, TDT[dt], fill=dev(case.v_cache, dt))
+    kc, vc = gk.t, gv.t
     pl = torch.from_numpy(case.prefix_len).cuda()
     so = torch.from_numpy(case.src_off).cuda()
     nb = vq.verify_attention_workspace_bytes(B, L, Hq, Hkv, D, S_cap)
     # the workspace needs no initial contents: start it as NaN bytes
     ws = torch.full((nb,), ws_fill, dtype=torch.uint8, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = torch.full_like(q, float("nan"))
+    go = Guarded(q.shape, q.dtype, fill=float("nan"))
+    out = go.t
     vq.verify_attention(q, kn, vn, kc, vc, pl, so, ws, rotary_dim, theta, scale, out=out,
                         status=status)
-    torch.cuda.synchronize()
+    for g in (gk, gv, go):
+        g.check()
     kco, vco = case.k_cache.copy(), case.v_cache.copy()
     r_out, r_krot, r_st = oracle.verify_attention(case.q, case.k_new, case.v_new, kco, vco,
                                                   case.prefix_len, case.src_off, ODT[dt],

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from parity import (ORACLE_DT, TOL, assert_proj_close, out_to_f64, proj_error, to_dev_act,
+from parity import (Guarded, ORACLE_DT, TOL, assert_proj_close, out_to_f64, proj_error, to_dev_act,
                     to_dev_weights)
 from speculative_block_draft_02_gb300 import binding as vq
 from speculative_block_draft_02_gb300 import synth
@@ -48,9 +48,10 @@ def run_linear(x_bits, w, dtype, ws=None):
     M, K = x.shape
     if ws is None:
         ws = _workspace(M, K, w.N, dtype)
-    y = vq.vq_linear(x, qw, s, b, workspace=ws)
-    torch.cuda.synchronize()
-    return out_to_f64(y)
+    y = Guarded((M, w.N), x.dtype, fill=float("nan"))
+    vq.vq_linear(x, qw, s, b, y=y.t, workspace=ws)
+    y.check()
+    return out_to_f64(y.t)
 
 
 def oracle_linear(x_bits, w, dtype, cols=None):
@@ -223,9 +224,10 @@ def run_vocab(x_bits, w, dtype="bf16"):
     qw, s, b = to_dev_weights(w)
     M = x.shape[0]
     ws = torch.zeros(vq.vq_vocab_argmax_workspace_bytes(M), dtype=torch.uint8, device="cuda")
-    mx = torch.empty(M, dtype=torch.float32, device="cuda")
-    idx, mx = vq.vq_vocab_argmax(x, qw, s, b, ws, maxval=mx)
-    torch.cuda.synchronize()
+    gi, gm = Guarded((M,), torch.int32, fill=-1), Guarded((M,), torch.float32, fill=float("nan"))
+    idx, mx = vq.vq_vocab_argmax(x, qw, s, b, ws, argmax=gi.t, maxval=gm.t)
+    gi.check()
+    gm.check()
     return idx.cpu().numpy(), mx.cpu().numpy(), ws
 
 
@@ -283,8 +285,11 @@ def run_vocab_top2(x_bits, w, dtype="bf16"):
     M = x.shape[0]
     ws = torch.zeros(vq.vq_vocab_argmax_top2_workspace_bytes(M), dtype=torch.uint8,
                      device="cuda")
-    idx, mx, sec = vq.vq_vocab_argmax_top2(x, qw, s, b, ws)
-    torch.cuda.synchronize()
+    gi, gm = Guarded((M,), torch.int32, fill=-1), Guarded((M,), torch.float32, fill=float("nan"))
+    gs = Guarded((M,), torch.float32, fill=float("nan"))
+    idx, mx, sec = vq.vq_vocab_argmax_top2(x, qw, s, b, ws, argmax=gi.t, maxval=gm.t, second=gs.t)
+    for g in (gi, gm, gs):
+        g.check()
     return idx.cpu().numpy(), mx.cpu().numpy(), sec.cpu().numpy(), ws, M
 
 
@@ -386,12 +391,16 @@ def _kv_to_dev(tensors):
 
 
 def _run_compact(case, max_keep=16):
-    dev = _kv_to_dev(case.tensors)
+    src = _kv_to_dev(case.tensors)
+    guarded = [Guarded(t.shape, t.dtype, fill=t) for t in src]
+    dev = [g.t for g in guarded]
+    del src
     i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     new_len = vq.kv_compact_per_row(dev, i32(case.prefix_len), i32(case.src_off), i32(case.keep),
                                     max_keep, status=status)
-    torch.cuda.synchronize()
+    for g in guarded:
+        g.check()
     return dev, new_len.cpu().numpy(), int(status.item())
 
 
