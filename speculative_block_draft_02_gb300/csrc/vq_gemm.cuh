@@ -83,16 +83,18 @@ __host__ __device__ constexpr int misc_bytes(bool argmax) { return argmax ? kMis
 // Work split of the consumers by the number MT of n8 tiles (M <= 8*MT):
 // TEAMS teams taking alternate stages, RT 16-row tiles per warp (the tiles
 // share the x fragments), KQ K-slices per stage within a team, GPW = 8/KQ
-// groups per warp and stage. WIDE (prepared slices, no K split): four row
-// tiles per warp and half the warps, so that each warp has four independent
-// MMA chains and, with 9 warps a block, up to 168 registers (17 warps cap
-// them at 96); measured 11.3 vs 12.0 us per headline call. With a K split,
-// whose units are one or two stages, the narrower split stays faster.
+// groups per warp and stage. WIDE (prepared slices, no K split): half the
+// warps, so that with 9 warps a block each has up to 168 registers (17 warps
+// cap them at 96); at M <= 8 four row tiles per warp (four independent MMA
+// chains; measured 11.3 vs 12.0 us per headline call), at M <= 16 two row
+// tiles over all 8 groups of a stage (the accumulators of four tiles x two n8
+// tiles spilled; 15.2 vs 17.0 us). With a K split, whose units are one or two
+// stages, the narrower split stays faster.
 template <int MT, bool WIDE = false>
 struct Cfg {
   static constexpr int TEAMS = MT <= 2 ? 2 : 1;   // a power of two
-  static constexpr int RT = (MT <= 2 && WIDE) ? 4 : (MT <= 2 ? 2 : 1);
-  static constexpr int KQ = MT <= 2 ? 2 : 1;
+  static constexpr int RT = (MT == 1 && WIDE) ? 4 : (MT <= 2 ? 2 : 1);
+  static constexpr int KQ = (MT == 2 && WIDE) ? 1 : (MT <= 2 ? 2 : 1);
   static constexpr int GPW = 8 / KQ;
   static constexpr int RW = 8 / RT;                 // warps along the rows
   static constexpr int WPT = RW * KQ;               // warps per team
