@@ -83,18 +83,21 @@ __host__ __device__ constexpr int misc_bytes(bool argmax) { return argmax ? kMis
 // Work split of the consumers by the number MT of n8 tiles (M <= 8*MT):
 // TEAMS teams taking alternate stages, RT 16-row tiles per warp (the tiles
 // share the x fragments), KQ K-slices per stage within a team, GPW = 8/KQ
-// groups per warp and stage. WIDE (prepared slices, no K split): half the
-// warps, so that with 9 warps a block each has up to 168 registers (17 warps
-// cap them at 96); at M <= 8 four row tiles per warp (four independent MMA
-// chains; measured 11.3 vs 12.0 us per headline call), at M <= 16 two row
-// tiles over all 8 groups of a stage (the accumulators of four tiles x two n8
-// tiles spilled; 15.2 vs 17.0 us). With a K split, whose units are one or two
-// stages, the narrower split stays faster.
-template <int MT, bool WIDE = false>
+// groups per warp and stage. WIDE != 0 (no K split): half the warps, so that
+// with 9 warps a block each has up to 168 registers (17 warps cap them at
+// 96). WIDE == 2 (prepared slices): each warp two row tiles over all 8 groups
+// of a stage; measured per call at K=5120, N=17408: M=8 10.6 us (four tiles
+// over four groups 10.8, two tiles over four groups with 17 warps 12.0), M=16
+// 15.2 us (four tiles over four groups spilled its accumulators: 17.0).
+// WIDE == 1 (x per stage by TMA: fp32 x, arg max): four row tiles over four
+// groups (two tiles over all eight measured 24.8 vs 22.8 us at fp32 M=8).
+// With a K split, whose units are one or two stages, the narrower split
+// stays faster.
+template <int MT, int WIDE = 0>
 struct Cfg {
   static constexpr int TEAMS = MT <= 2 ? 2 : 1;   // a power of two
-  static constexpr int RT = (MT == 1 && WIDE) ? 4 : (MT <= 2 ? 2 : 1);
-  static constexpr int KQ = (MT == 2 && WIDE) ? 1 : (MT <= 2 ? 2 : 1);
+  static constexpr int RT = (MT <= 2 && WIDE == 1) ? 4 : (MT <= 2 ? 2 : 1);
+  static constexpr int KQ = (MT <= 2 && WIDE != 2) ? 2 : 1;
   static constexpr int GPW = 8 / KQ;
   static constexpr int RW = 8 / RT;                 // warps along the rows
   static constexpr int WPT = RW * KQ;               // warps per team
@@ -422,7 +425,7 @@ struct LaneOffsets {
   uint32_t xs;              // (first group of the slice, row 2t) in the group-sum table, bytes
 };
 
-template <int ACT, int MT, bool WIDE>
+template <int ACT, int MT, int WIDE>
 __device__ __forceinline__ LaneOffsets<ACT, MT> lane_offsets(int rw, int kq, int g, int t) {
   using C = Cfg<MT, WIDE>;
   constexpr int MP = 8 * MT;
@@ -469,7 +472,7 @@ __device__ __forceinline__ Packed<GPW> lds_packed_at(uint32_t a) {
 // weight row 16r + 2i + 1. sb is the stage's shared address, xsb the group-sum
 // table's shared address for the stage's first group. All per-tile, per-group
 // and per-row offsets are load immediates.
-template <int ACT, int MT, bool WIDE>
+template <int ACT, int MT, int WIDE>
 __device__ __forceinline__ void consume_stage(uint32_t sb, uint32_t xsb,
                                               const LaneOffsets<ACT, MT>& o,
                                               float (&tot)[Cfg<MT, WIDE>::RT][MT][4]) {
@@ -948,7 +951,7 @@ struct XsLane {
   uint32_t inv;             // 1/f of rows 2t, 2t+1
 };
 
-template <int MT, bool WIDE>
+template <int MT, int WIDE>
 __device__ __forceinline__ XsLane xs_lane(int rw, int kq, int g, int t) {
   using C = Cfg<MT, WIDE>;
   XsLane o;
@@ -971,7 +974,7 @@ __device__ __forceinline__ XsLane xs_lane(int rw, int kq, int g, int t) {
 // the warp's K-slice of groups for its RT row tiles, folded in each slice's
 // scaled units and then brought back with the slice's 1/f. The codes are
 // unpacked once per row tile and serve every n8 tile.
-template <int ACT, int MT, bool WIDE>
+template <int ACT, int MT, int WIDE>
 __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
                                                  float (&tot)[Cfg<MT, WIDE>::RT][MT][4]) {
   using C = Cfg<MT, WIDE>;
@@ -1076,7 +1079,7 @@ __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
   });
 }
 
-template <int ACT, int MT, bool ARGMAX, int XM, bool WIDE = false>
+template <int ACT, int MT, bool ARGMAX, int XM, int WIDE = 0>
 __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
     vq_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_x,
@@ -1391,7 +1394,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
 
     if constexpr (!ARGMAX) {
       // (the WIDE layout is only launched without a K split)
-      if (WIDE || p.S == 1) {
+      if (WIDE != 0 || p.S == 1) {
         if (!aborted) {
 #pragma unroll
           for (int r = 0; r < RT; ++r)
@@ -1588,7 +1591,7 @@ int launch_pdl(Kern k, dim3 grid, int threads, size_t smem, cudaStream_t stream,
   return cudaLaunchKernelEx(&cfg, k, args...) == cudaSuccess ? VQ_OK : VQ_ECUDA;
 }
 
-template <int ACT, int MT, bool AM, int XM = 0, bool WIDE = false>
+template <int ACT, int MT, bool AM, int XM = 0, int WIDE = 0>
 int launch_one(const GemmLaunch& L) {
   auto k = vq_gemm_kernel<ACT, MT, AM, XM, WIDE>;
   if (ensure_smem<vq_gemm_kernel<ACT, MT, AM, XM, WIDE>>(L.smem) != VQ_OK) return VQ_ECUDA;
@@ -1630,8 +1633,8 @@ int launch_gemm_act(const GemmLaunch& L) {
     if (L.p.xm == 2) {
       if (L.MT > 2 || L.argmax) return VQ_EUNSUPPORTED;
       if (L.MT == 2)
-        return L.p.S == 1 ? launch_one<ACT, 2, false, 2, true>(L) : launch_one<ACT, 2, false, 2>(L);
-      return L.p.S == 1 ? launch_one<ACT, 1, false, 2, true>(L) : launch_one<ACT, 1, false, 2>(L);
+        return L.p.S == 1 ? launch_one<ACT, 2, false, 2, 2>(L) : launch_one<ACT, 2, false, 2>(L);
+      return L.p.S == 1 ? launch_one<ACT, 1, false, 2, 2>(L) : launch_one<ACT, 1, false, 2>(L);
     }
     if (L.p.xm == 3) {
       switch (L.MT) {
