@@ -454,6 +454,11 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
 
 int num_sms_current_device(int* out) { return device_state(out, nullptr); }
 int device_error_word(int32_t** out) { return device_state(nullptr, out); }
+int encode_rows_sw128(CUtensorMap* m, const void* ptr, uint64_t row_elems, uint64_t rows,
+                      uint32_t box_rows) {
+  return encode_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, ptr, row_elems, rows, row_elems * 2, 64,
+                   box_rows, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+}
 
 }  // namespace vq
 

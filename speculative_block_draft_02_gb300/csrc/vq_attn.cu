@@ -62,7 +62,8 @@ struct AttnParams {
   int32_t* err;     // the library's status word (a wait that gave up)
   float* part_o;    // [B][Hkv][RG][NC][64][D]   unnormalised chunk outputs
   float2* part_ml;  // [B][Hkv][RG][NC][64]      (max in log2 units, sum)
-  uint16_t* q_rot;  // [B][L][Hq][D]              rotated, rounded queries
+  uint16_t* q_rot;  // [B][Hkv][RG][64][D] rotated, rounded queries, one swizzled tile
+                    // per (row, KV head, group of 64 query rows) (sw_off layout)
   int L, Hq, Hkv, G, R, RG, NC, S_cap, rot_half;
   float scale_log2;                  // scale * log2(e)
   float2 inv_freq[kMaxRotPairs];     // (hi, lo): hi + lo = theta^(-2i / rotary_dim)
@@ -93,6 +94,30 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
   const uint16_t ha = f2h<kF16>(a), hb = f2h<kF16>(b);
   hi = (uint32_t)ha | ((uint32_t)hb << 16);
   lo = (uint32_t)f2h<kF16>(a - h2f<kF16>(ha)) | ((uint32_t)f2h<kF16>(b - h2f<kF16>(hb)) << 16);
+}
+
+// 16 bytes global -> shared (at a shared-space address) without a register
+// round trip; zeros when !valid (nothing is read then).
+__device__ __forceinline__ void cp_async_16s(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void sts128_zero(uint32_t addr) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Byte offset of element (row, col) of a [64 rows][D] 16-bit tile kept as D/64
+// segments of [64 rows][128 B] in the 128-byte swizzle (the layout a 2-D TMA
+// box of 64 x 64 values with SWIZZLE_128B lands in): 16-byte piece c of a
+// segment's row r sits at piece c ^ (r % 8). col is a multiple of 8.
+__device__ __forceinline__ uint32_t sw_off(int row, int col) {
+  return (uint32_t)((col >> 6) * 8192 + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4));
 }
 
 __device__ __forceinline__ bool row_in_range(int P, int S, int L, int S_cap) {
@@ -135,8 +160,9 @@ __global__ void __launch_bounds__(kRopeThreads)
     if (r < p.Hq + p.Hkv) return p.k_new + (((size_t)b * p.L + j) * p.Hkv + (r - p.Hq)) * D;
     return p.v_new + (((size_t)b * p.L + j) * p.Hkv + (r - p.Hq - p.Hkv)) * D;
   };
+  // key and value rows go to cache slot S + j; query head hq to row
+  // rr = j * G + (hq - hk * G) of its group's tile
   auto row_dst = [&](int r) -> uint16_t* {
-    if (r < p.Hq) return p.q_rot + (((size_t)b * p.L + j) * p.Hq + r) * D;
     const int h = r < p.Hq + p.Hkv ? r - p.Hq : r - p.Hq - p.Hkv;
     uint16_t* cache = r < p.Hq + p.Hkv ? p.k_cache : p.v_cache;
     return cache + (((size_t)b * p.Hkv + h) * p.S_cap + (S + j)) * D;
@@ -166,8 +192,17 @@ __global__ void __launch_bounds__(kRopeThreads)
     __syncthreads();
     for (int i = tid; i < nr * DC; i += kRopeThreads) {
       const int rl = i / DC, c = i - rl * DC;
-      reinterpret_cast<uint4*>(row_dst(r0 + rl))[c] =
-          *reinterpret_cast<const uint4*>(tile + rl * D + c * 8);
+      const int r = r0 + rl;
+      const uint4 v = *reinterpret_cast<const uint4*>(tile + rl * D + c * 8);
+      if (r < p.Hq) {
+        const int hk = r / p.G, rr = j * p.G + (r - hk * p.G);
+        const int rg = rr / kAttnRows, row = rr - rg * kAttnRows;
+        uint8_t* t = reinterpret_cast<uint8_t*>(p.q_rot) +
+                     (((size_t)b * p.Hkv + hk) * p.RG + rg) * (size_t)(kAttnRows * D * 2);
+        *reinterpret_cast<uint4*>(t + sw_off(row, c * 8)) = v;
+      } else {
+        reinterpret_cast<uint4*>(row_dst(r))[c] = v;
+      }
     }
   }
 }
@@ -183,14 +218,15 @@ __device__ __forceinline__ bool attn_wait(uint32_t bar) {
 
 template <bool kF16, int D>
 __global__ void __launch_bounds__(kAttnThreads, 4)
-    verify_attn_partial_kernel(const __grid_constant__ AttnParams p) {
-  constexpr int QS = D + 8;               // row stride of the tiles (16-bit elements)
-  constexpr uint32_t RB = D * 2;          // bytes of one row
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);   // [64][QS] rotated queries
-  uint16_t* Ks = Qs + kAttnRows * QS;                  // [64][QS] keys
-  uint16_t* Vs = Ks + kChunk * QS;                     // [64][QS] values
-  const uint32_t bar_pre = smem_addr(Vs + kChunk * QS), bar_rest = bar_pre + 8u;
+    verify_attn_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
+                               const __grid_constant__ CUtensorMap tm_v,
+                               const __grid_constant__ AttnParams p) {
+  constexpr uint32_t TILE = kAttnRows * D * 2;   // bytes of a 64-row tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t Qs = (raw + 1023u) & ~1023u;   // the swizzle wants 1 KiB-aligned tiles
+  const uint32_t Ks = Qs + TILE, Vs = Qs + 2 * TILE;
+  const uint32_t bar_pre = Qs + 3 * TILE, bar_rest = bar_pre + 8u;
 
   const int chunk = blockIdx.x;
   const int hk = blockIdx.y / p.RG, rg = blockIdx.y % p.RG;
@@ -210,59 +246,67 @@ __global__ void __launch_bounds__(kAttnThreads, 4)
   __syncthreads();
 
   // Key tl of the chunk (t = c0 + tl) sits in cache slot t below P and in slot
-  // S + (t - P) from P on. Rows arrive by bulk copies, one per row: the prefix
-  // rows are requested before the wait for the rotation kernel (which writes
-  // only slots S.. and the rotated queries; everything before it in the stream
-  // had completed when it started), the queries and the block's rows after it.
+  // S + (t - P) from P on. The chunk's rows from slot c0 on arrive as 2-D TMA
+  // boxes of 64 rows x 64 values (two per tile at D = 128), requested before
+  // the wait for the rotation kernel (which writes only slots S.. and the
+  // rotated queries; everything before it in the stream had completed when it
+  // started); that is the whole chunk when it lies in the prefix. In a chunk
+  // that reaches the block, the rows from P on are then replaced, once the
+  // boxes have landed: the block's keys and values (slots S..) 16 bytes at a
+  // time into the same swizzled layout, zeros past T. The group's rotated
+  // queries are one tile of the workspace: one bulk copy after the wait.
+  const bool whole = c0 + kChunk <= P;
+  const int n_pre = max(0, min(P - c0, kChunk));   // prefix rows: tl < n_pre
+  const int n_vis = min(T - c0, kChunk);           // visible rows: tl < n_vis
   const size_t head = ((size_t)b * p.Hkv + hk) * p.S_cap;
-  const int n_pre = max(0, min(P - c0, kChunk));   // prefix keys: tl < n_pre
-  const int n_vis = min(T - c0, kChunk);           // visible keys: tl < n_vis
-  const int nq = min(kAttnRows, p.R - rg * kAttnRows);
-  if (tid < 32) {
-    if (tid == 0) mbar_arrive_expect_tx(bar_pre, 2u * (uint32_t)n_pre * RB);
-    __syncwarp();
-    for (int tl = tid; tl < n_pre; tl += 32) {
-      const size_t slot = head + (size_t)(c0 + tl);
-      bulk_load(smem_addr(Ks + tl * QS), p.k_cache + slot * D, RB, bar_pre);
-      bulk_load(smem_addr(Vs + tl * QS), p.v_cache + slot * D, RB, bar_pre);
+  if (tid == 0) {
+    if (n_pre > 0) {
+      mbar_arrive_expect_tx(bar_pre, 2u * TILE);
+#pragma unroll
+      for (int sg = 0; sg < D / 64; ++sg) {
+        tma_load_2d(Ks + sg * 8192, &tm_k, sg * 64, (int)(head + c0), bar_pre);
+        tma_load_2d(Vs + sg * 8192, &tm_v, sg * 64, (int)(head + c0), bar_pre);
+      }
+    } else {
+      mbar_arrive(bar_pre);
     }
   }
   grid_wait_prerequisites();
-  if (tid < 32) {
-    if (tid == 0) mbar_arrive_expect_tx(bar_rest, (uint32_t)(2 * (n_vis - n_pre) + nq) * RB);
-    __syncwarp();
-    for (int tl = n_pre + tid; tl < n_vis; tl += 32) {
-      const size_t slot = head + (size_t)(S + (c0 + tl - P));
-      bulk_load(smem_addr(Ks + tl * QS), p.k_cache + slot * D, RB, bar_rest);
-      bulk_load(smem_addr(Vs + tl * QS), p.v_cache + slot * D, RB, bar_rest);
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_rest, TILE);
+    bulk_load(Qs,
+              reinterpret_cast<const uint8_t*>(p.q_rot) +
+                  (((size_t)b * p.Hkv + hk) * p.RG + rg) * (size_t)TILE,
+              TILE, bar_rest);
+  }
+  bool ok = true;
+  if (!whole) {
+    ok = attn_wait(bar_pre);   // the boxes' rows past n_pre are replaced next
+    if (ok) {
+      for (int i = tid; i < (n_vis - n_pre) * (D / 8); i += kAttnThreads) {
+        const int tl = n_pre + i / (D / 8), c = i % (D / 8);
+        const size_t slot = head + (size_t)(S + (c0 + tl - P));
+        const uint32_t o = sw_off(tl, c * 8);
+        cp_async_16s(Ks + o, p.k_cache + slot * D + c * 8, true);
+        cp_async_16s(Vs + o, p.v_cache + slot * D + c * 8, true);
+      }
+      for (int i = tid; i < (kChunk - n_vis) * (D / 8); i += kAttnThreads) {
+        const int tl = n_vis + i / (D / 8), c = i % (D / 8);
+        const uint32_t o = sw_off(tl, c * 8);
+        sts128_zero(Ks + o);
+        sts128_zero(Vs + o);
+      }
+      cp_async_wait_all();
     }
-    // query row r = j * G + (hq - hk * G) of the group
-    for (int r = tid; r < nq; r += 32) {
-      const int rr = rg * kAttnRows + r;
-      const int j = rr / p.G, hq = hk * p.G + (rr - j * p.G);
-      bulk_load(smem_addr(Qs + r * QS), p.q_rot + (((size_t)b * p.L + j) * p.Hq + hq) * D, RB,
-                bar_rest);
-    }
   }
-  // rows no copy fills: keys past the last visible one (their values must be
-  // finite, as their probabilities are 0) and query rows past the group's
-  for (int i = tid; i < (kChunk - n_vis) * (D / 8); i += kAttnThreads) {
-    const int tl = n_vis + i / (D / 8), c = i % (D / 8);
-    *reinterpret_cast<uint4*>(Ks + tl * QS + c * 8) = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(Vs + tl * QS + c * 8) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  for (int i = tid; i < (kAttnRows - nq) * (D / 8); i += kAttnThreads) {
-    const int r = nq + i / (D / 8), c = i % (D / 8);
-    *reinterpret_cast<uint4*>(Qs + r * QS + c * 8) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (!attn_wait(bar_pre) || !attn_wait(bar_rest)) {
+  if (!ok || !attn_wait(bar_pre) || !attn_wait(bar_rest)) {
     // give up: report it, let the copies already issued land, and leave
     if (tid == 0) atomicOr(p.err, kErrWaitTimeout);
     attn_wait(bar_pre);
     attn_wait(bar_rest);
     return;
   }
-  __syncthreads();   // the zero rows too
+  __syncthreads();   // the gathered rows too
 
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
   const int row0 = warp * 16;
@@ -276,17 +320,16 @@ __global__ void __launch_bounds__(kAttnThreads, 4)
   float sc[8][4];
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-  const uint32_t qa_addr = smem_addr(Qs + (row0 + (lane & 15)) * QS + (lane >> 4) * 8);
-  const uint32_t kb_addr =
-      smem_addr(Ks + ((lane & 7) + ((lane >> 4) << 3)) * QS + ((lane >> 3) & 1) * 8);
+  const int qa_row = row0 + (lane & 15), qa_col = (lane >> 4) * 8;
+  const int kb_row = (lane & 7) + ((lane >> 4) << 3), kb_col = ((lane >> 3) & 1) * 8;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     uint32_t qa[4];
-    ldsm_x4(qa, qa_addr + ks * 32);
+    ldsm_x4(qa, Qs + sw_off(qa_row, ks * 16 + qa_col));
 #pragma unroll
     for (int np = 0; np < 4; ++np) {
       uint32_t kb[4];
-      ldsm_x4(kb, kb_addr + (np * 16 * QS + ks * 16) * 2);
+      ldsm_x4(kb, Ks + sw_off(np * 16 + kb_row, ks * 16 + kb_col));
       mma_16816<kF16>(sc[2 * np], qa, kb[0], kb[1]);
       mma_16816<kF16>(sc[2 * np + 1], qa, kb[2], kb[3]);
     }
@@ -330,8 +373,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4)
   // would move the outputs by up to 2^-9 relative, so there P is split into a
   // high part and the remainder (two MMAs, about 16 bits); fp16's 11 bits
   // suffice alone. B fragments of two 8-dimension tiles per ldmatrix.x4.trans.
-  const uint32_t vb_addr =
-      smem_addr(Vs + ((lane & 7) + ((lane >> 3) & 1) * 8) * QS + (lane >> 4) * 8);
+  const int vb_row = (lane & 7) + ((lane >> 3) & 1) * 8, vb_col = (lane >> 4) * 8;
 #pragma unroll
   for (int kk = 0; kk < kChunk / 16; ++kk) {
     uint32_t ah[4], al[4];
@@ -353,7 +395,7 @@ __global__ void __launch_bounds__(kAttnThreads, 4)
 #pragma unroll
     for (int np = 0; np < D / 16; ++np) {
       uint32_t vb[4];
-      ldsm_x4_t(vb, vb_addr + (kk * 16 * QS + np * 16) * 2);
+      ldsm_x4_t(vb, Vs + sw_off(kk * 16 + vb_row, np * 16 + vb_col));
       mma_16816<kF16>(o[2 * np], ah, vb[0], vb[1]);
       mma_16816<kF16>(o[2 * np + 1], ah, vb[2], vb[3]);
       if constexpr (!kF16) {
@@ -476,7 +518,9 @@ int attn_check(const void* q, const void* k_new, const void* v_new, const void* 
   if (L > kMaxBlock || S_cap > kMaxCap) return VQ_EUNSUPPORTED;
   // grid limits: (chunks, Hkv x row groups, B) and (L x Hq, B)
   const long long row_groups = ((long long)L * (Hq / Hkv) + kAttnRows - 1) / kAttnRows;
-  if ((long long)Hkv * row_groups > 65535 || B > 65535 || (long long)L * Hq > 0x7fffffffll)
+  // (the cache rows are addressed by 32-bit TMA coordinates)
+  if ((long long)Hkv * row_groups > 65535 || B > 65535 || (long long)L * Hq > 0x7fffffffll ||
+      (long long)B * Hkv * S_cap > 0x7fffffffll)
     return VQ_EUNSUPPORTED;
   const uintptr_t a16 = (uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new |
                         (uintptr_t)k_cache | (uintptr_t)v_cache;
@@ -509,9 +553,10 @@ size_t attn_qrot_offset(size_t rows, int D) {
 }
 
 template <bool kF16, int D>
-int attn_launch(const AttnParams& p, int B, cudaStream_t stream) {
-  // the three tiles and two mbarriers
-  const size_t smem = (size_t)(kAttnRows + 2 * kChunk) * (D + 8) * 2 + 16;
+int attn_launch(const AttnParams& p, int B, cudaStream_t stream, const CUtensorMap& tm_k,
+                const CUtensorMap& tm_v) {
+  // three swizzled tiles (1 KiB-aligned) and two mbarriers
+  const size_t smem = 1024 + (size_t)3 * kAttnRows * D * 2 + 16;
   auto* partial = verify_attn_partial_kernel<kF16, D>;
   if (ensure_smem<verify_attn_partial_kernel<kF16, D>>(smem) != VQ_OK) return VQ_ECUDA;
   // the rotation runs after everything before it in the stream; the partial
@@ -529,7 +574,7 @@ int attn_launch(const AttnParams& p, int B, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, partial, p) != cudaSuccess) return VQ_ECUDA;
+    if (cudaLaunchKernelEx(&cfg, partial, tm_k, tm_v, p) != cudaSuccess) return VQ_ECUDA;
   }
   // the merge may be scheduled while the partial kernel runs; it waits for it
   // (griddepcontrol.wait) before reading anything
@@ -559,7 +604,7 @@ extern "C" size_t verify_attention_workspace_bytes(int B, int L, int Hq, int Hkv
   const AttnShape s = attn_shape(L, Hq, Hkv, S_cap);
   const size_t rows = attn_part_count(B, Hkv, s);
   // [partial outputs][partial (max, sum)][rotated queries], each 16-byte aligned
-  return attn_qrot_offset(rows, D) + (size_t)B * L * Hq * D * sizeof(uint16_t);
+  return attn_qrot_offset(rows, D) + (size_t)B * Hkv * s.RG * kAttnRows * D * sizeof(uint16_t);
 }
 
 extern "C" int verify_attention(const void* q, const void* k_new, const void* v_new,
@@ -609,7 +654,17 @@ extern "C" int verify_attention(const void* q, const void* k_new, const void* v_
     const float hi = (float)f;
     p.inv_freq[i] = make_float2(hi, (float)(f - (double)hi));
   }
+  // the caches as rows of D values, boxes of 64 rows x 64 values (cached per
+  // host thread, so a call on the same caches encodes nothing)
+  CUtensorMap tm_k, tm_v;
+  const uint64_t kv_rows = (uint64_t)B * Hkv * S_cap;
+  if (encode_rows_sw128(&tm_k, k_cache, (uint64_t)D, kv_rows, kChunk) != VQ_OK ||
+      encode_rows_sw128(&tm_v, v_cache, (uint64_t)D, kv_rows, kChunk) != VQ_OK)
+    return VQ_ECUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (dtype == VQ_F16) return D == 64 ? attn_launch<true, 64>(p, B, st) : attn_launch<true, 128>(p, B, st);
-  return D == 64 ? attn_launch<false, 64>(p, B, st) : attn_launch<false, 128>(p, B, st);
+  if (dtype == VQ_F16)
+    return D == 64 ? attn_launch<true, 64>(p, B, st, tm_k, tm_v)
+                   : attn_launch<true, 128>(p, B, st, tm_k, tm_v);
+  return D == 64 ? attn_launch<false, 64>(p, B, st, tm_k, tm_v)
+                 : attn_launch<false, 128>(p, B, st, tm_k, tm_v);
 }

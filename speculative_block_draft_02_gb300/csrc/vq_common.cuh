@@ -246,6 +246,12 @@ namespace vq {
 int num_sms_current_device(int* out);
 // The device's status word (kErrWaitTimeout ...) for kernels that report into it.
 int device_error_word(int32_t** out);
+// A 2-D tensor map over rows of 16-bit values (row_elems a multiple of 64,
+// 16-byte aligned rows): boxes of 64 values x box_rows rows in the 128-byte
+// swizzle (16-byte piece c of row r of a box lands at piece c ^ (r % 8)).
+// The device's state must have been set up (device_error_word) first.
+int encode_rows_sw128(CUtensorMap* m, const void* ptr, uint64_t row_elems, uint64_t rows,
+                      uint32_t box_rows);
 
 // Raises kernel K's dynamic shared-memory limit on the current device to at
 // least `bytes`, calling the runtime only the first time a device needs a

@@ -118,13 +118,14 @@ def test_host_validation_rejects_before_any_launch(vqlib):
 def test_verify_attention_workspace_and_host_validation(vqlib):
     P = ctypes.c_void_p
     # rows of partial results: B * Hkv * ceil(L*G/64) * ceil(S_cap/64) * 64, each
-    # D floats of output plus (max, sum); then the rotated queries, B*L*Hq*D 16-bit
+    # D floats of output plus (max, sum); then the rotated queries as one tile
+    # of 64 rows x D 16-bit values per (row, KV head, group of 64 query rows)
     rows = 4 * 8 * 1 * 32 * 64
     assert vqlib.verify_attention_workspace_bytes(4, 16, 32, 8, 128, 2048) == \
-        rows * (128 * 4 + 8) + 4 * 16 * 32 * 128 * 2
+        rows * (128 * 4 + 8) + 4 * 8 * 1 * 64 * 128 * 2
     rows = 2 * 2 * 2 * 2 * 64                      # L*G = 80 rows -> two groups of 64
     assert vqlib.verify_attention_workspace_bytes(2, 10, 16, 2, 64, 100) == \
-        rows * (64 * 4 + 8) + 2 * 10 * 16 * 64 * 2
+        rows * (64 * 4 + 8) + 2 * 2 * 2 * 64 * 64 * 2
     assert vqlib.verify_attention_workspace_bytes(2, 10, 15, 2, 64, 100) == 0
 
     fake = P(0x1000)
