@@ -109,7 +109,7 @@ def check(case, res):
 
 # (B, L, Hq, Hkv, D, S_cap, prefix_len, src_off, dtype, rotary_dim, theta)
 CASES = [
-    # three rows: no prefix, a gap, none; several chunks of 128 with ragged tails
+    # three rows: no prefix, a gap, none; several 64-key chunks with ragged tails
     (3, 16, 8, 2, 128, 520, [0, 137, 300], None, "f16", 128, 1e6),
     # block ends at the cache end; src_off per row; partial rotation; bf16; D 64
     (2, 8, 4, 4, 64, 300, [129, 255], [200, 292], "bf16", 32, 1e4),
@@ -121,6 +121,9 @@ CASES = [
     (4, 64, 8, 8, 128, 1024, [900, 3, 500, 128], None, "bf16", 128, 1e6),
     # prefix lengths on chunk edges (127, 128, 129) with the block after them
     (3, 16, 4, 2, 128, 400, [127, 128, 129], [127, 150, 300], "f16", 96, 5e5),
+    # a chunk that reaches the block near the cache end: its 64-row box of the
+    # last KV head runs past the end of the cache tensor (zero-filled rows)
+    (1, 8, 4, 2, 64, 100, [90], [92], "f16", 64, 1e4),
 ]
 
 
