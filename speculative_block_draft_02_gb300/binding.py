@@ -16,6 +16,10 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libvq.so")
+# The same kernels built with -DVQ_CHECK_BOUNDS: every global store (and the
+# gathers that have no hardware bounds) is tested against its buffer's extent,
+# a miss is skipped and sets bit 1 of the device status word (vq_device_error).
+CHECKED_LIB_PATH = os.path.join(_HERE, "libvq_checked.so")
 
 VQ_BF16, VQ_F16, VQ_F32 = 0, 1, 2
 _ACT = {torch.bfloat16: VQ_BF16, torch.float16: VQ_F16, torch.float32: VQ_F32}
@@ -54,6 +58,19 @@ class VQError(RuntimeError):
     pass
 
 
+def open_library(path: str) -> ctypes.CDLL:
+    """Loads a build of the library at `path` and declares every signature."""
+    if not os.path.exists(path):
+        raise VQError("CUDA library %s is missing: build it with "
+                      "speculative_block_draft_02_gb300.build.build()" % path)
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib() -> ctypes.CDLL:
     """The loaded CUDA library. Raises if it has not been built."""
     global _lib
@@ -61,15 +78,7 @@ def lib() -> ctypes.CDLL:
         return _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise VQError("CUDA library %s is missing: build it with "
-                              "speculative_block_draft_02_gb300.build.build()" % LIB_PATH)
-            handle = ctypes.CDLL(LIB_PATH)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(handle, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = handle
+            _lib = open_library(LIB_PATH)
     return _lib
 
 

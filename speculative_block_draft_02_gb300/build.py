@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libvq.so")
+# the bounds-checked build (VQ_CHECK_BOUNDS): same sources, its own objects
+BUILD_CHECKED = os.path.join(PKG, "_build", "checked")
+LIB_CHECKED = os.path.join(PKG, "libvq_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -39,21 +42,26 @@ def _deps():
         os.path.join(INCLUDE, "vq.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), checked: bool = False) -> str:
+    """Compiles and links the library; `checked` builds libvq_checked.so, in
+    which every kernel store is tested against its buffer's extent."""
+    lib, objdir = (LIB_CHECKED, BUILD_CHECKED) if checked else (LIB, BUILD)
+    if checked:
+        extra = (*extra, "-DVQ_CHECK_BOUNDS")
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,14 +72,15 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".%d.tmp" % os.getpid()
+    tmp = lib + ".%d.tmp" % os.getpid()
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
-    print(build(force=True, verbose=v, extra=["-Xptxas", "-v"] if v else []))
+    print(build(force=True, verbose=v, extra=["-Xptxas", "-v"] if v else [],
+                checked="--checked" in sys.argv))

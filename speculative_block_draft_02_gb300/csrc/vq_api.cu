@@ -382,6 +382,9 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
   p.tab_bytes = pl.tab_bytes;
   p.y = y;
   p.err = err;
+  // extents for bounds-checked builds, from the sizes of the call and of the
+  // workspace the caller passed (not from the plan's own counts)
+  p.y_elems = (size_t)M * N;
   if (argmax) {
     p.keys = static_cast<unsigned long long*>(ws);
     p.done = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + (size_t)M * 8);
@@ -389,13 +392,17 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
     p.maxval = maxval;
     if (second) {
       p.second = second;
-      p.cand = reinterpret_cast<uint4*>(static_cast<char*>(ws) + round_up((size_t)M * 8 + 4, 16));
+      const size_t off = round_up((size_t)M * 8 + 4, 16);
+      p.cand = reinterpret_cast<uint4*>(static_cast<char*>(ws) + off);
+      p.cand_elems = ws_bytes > off ? (ws_bytes - off) / 16 : 0;
     }
   } else {
     if (pl.ws_xp_bytes) p.xprep = ws;
     if (pl.S > 1) {
       p.cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + pl.ws_xp_bytes);
       p.part = reinterpret_cast<float*>(static_cast<char*>(ws) + pl.ws_xp_bytes + pl.ws_cnt_bytes);
+      const size_t off = pl.ws_xp_bytes + pl.ws_cnt_bytes;
+      p.part_elems = ws_bytes > off ? (ws_bytes - off) / 4 : 0;
     }
   }
 

@@ -64,6 +64,7 @@ struct AttnParams {
   float2* part_ml;  // [B][Hkv][RG][NC][64]      (max in log2 units, sum)
   uint16_t* q_rot;  // [B][Hkv][RG][64][D] rotated, rounded queries, one swizzled tile
                     // per (row, KV head, group of 64 query rows) (sw_off layout)
+  size_t cache_elems, out_elems, part_rows, qrot_bytes;   // extents (bounds-checked builds)
   int L, Hq, Hkv, G, R, RG, NC, S_cap, rot_half;
   float scale_log2;                  // scale * log2(e)
   float2 inv_freq[kMaxRotPairs];     // (hi, lo): hi + lo = theta^(-2i / rotary_dim)
@@ -197,11 +198,14 @@ __global__ void __launch_bounds__(kRopeThreads)
       if (r < p.Hq) {
         const int hk = r / p.G, rr = j * p.G + (r - hk * p.G);
         const int rg = rr / kAttnRows, row = rr - rg * kAttnRows;
-        uint8_t* t = reinterpret_cast<uint8_t*>(p.q_rot) +
-                     (((size_t)b * p.Hkv + hk) * p.RG + rg) * (size_t)(kAttnRows * D * 2);
-        *reinterpret_cast<uint4*>(t + sw_off(row, c * 8)) = v;
+        const size_t off = (((size_t)b * p.Hkv + hk) * p.RG + rg) * (size_t)(kAttnRows * D * 2) +
+                           sw_off(row, c * 8);
+        if (in_bounds(off, p.qrot_bytes, p.err))
+          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.q_rot) + off) = v;
       } else {
-        reinterpret_cast<uint4*>(row_dst(r))[c] = v;
+        uint16_t* d = row_dst(r) + c * 8;
+        if (in_bounds((size_t)(d - (r < p.Hq + p.Hkv ? p.k_cache : p.v_cache)), p.cache_elems, p.err))
+          *reinterpret_cast<uint4*>(d) = v;
       }
     }
   }
@@ -287,8 +291,9 @@ __global__ void __launch_bounds__(kAttnThreads, 4)
         const int tl = n_pre + i / (D / 8), c = i % (D / 8);
         const size_t slot = head + (size_t)(S + (c0 + tl - P));
         const uint32_t o = sw_off(tl, c * 8);
-        cp_async_16s(Ks + o, p.k_cache + slot * D + c * 8, true);
-        cp_async_16s(Vs + o, p.v_cache + slot * D + c * 8, true);
+        const bool in = in_bounds(slot * D + c * 8, p.cache_elems, p.err);
+        cp_async_16s(Ks + o, p.k_cache + (in ? slot * D + c * 8 : 0), in);
+        cp_async_16s(Vs + o, p.v_cache + (in ? slot * D + c * 8 : 0), in);
       }
       for (int i = tid; i < (kChunk - n_vis) * (D / 8); i += kAttnThreads) {
         const int tl = n_vis + i / (D / 8), c = i % (D / 8);
@@ -412,13 +417,15 @@ __global__ void __launch_bounds__(kAttnThreads, 4)
   float* po = p.part_o + part * kAttnRows * D;
   float2* pml = p.part_ml + part * kAttnRows;
   const int lA = row0 + g, lB = lA + 8;
-  if (okA) {
+  const bool stA = okA && in_bounds(part * kAttnRows + lA, p.part_rows, p.err);
+  const bool stB = okB && in_bounds(part * kAttnRows + lB, p.part_rows, p.err);
+  if (stA) {
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd)
       *reinterpret_cast<float2*>(po + lA * D + nd * 8 + 2 * tq) = make_float2(o[nd][0], o[nd][1]);
     if (tq == 0) pml[lA] = make_float2(m[0], l[0]);
   }
-  if (okB) {
+  if (stB) {
 #pragma unroll
     for (int nd = 0; nd < D / 8; ++nd)
       *reinterpret_cast<float2*>(po + lB * D + nd * 8 + 2 * tq) = make_float2(o[nd][2], o[nd][3]);
@@ -438,7 +445,9 @@ __global__ void __launch_bounds__(D) verify_attn_combine_kernel(const __grid_con
   const int j = jh / p.Hq, hq = jh - j * p.Hq;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   grid_wait_prerequisites();   // launched early (programmatic serialization)
-  uint16_t* dst = p.out + (((size_t)b * p.L + j) * p.Hq + hq) * D;
+  const size_t dst_off = (((size_t)b * p.L + j) * p.Hq + hq) * D;
+  if (!in_bounds(dst_off + D - 1, p.out_elems, p.err)) return;
+  uint16_t* dst = p.out + dst_off;
   const int P = p.prefix_len[b], S = p.src_off[b];
   if (!row_in_range(P, S, p.L, p.S_cap)) {
     dst[tid] = 0;
@@ -639,6 +648,10 @@ extern "C" int verify_attention(const void* q, const void* k_new, const void* v_
   p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
                                         rows * (size_t)D * sizeof(float));
   p.q_rot = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + attn_qrot_offset(rows, D));
+  p.cache_elems = (size_t)B * Hkv * S_cap * D;
+  p.out_elems = (size_t)B * L * Hq * D;
+  p.part_rows = rows;
+  p.qrot_bytes = (size_t)B * Hkv * s.RG * kAttnRows * D * sizeof(uint16_t);
   p.L = L;
   p.Hq = Hq;
   p.Hkv = Hkv;

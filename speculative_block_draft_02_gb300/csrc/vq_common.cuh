@@ -18,7 +18,22 @@ namespace vq {
 // kernel argument) instead of trapping; vq_device_error() reads it.
 enum : int32_t {
   kErrWaitTimeout = 1 << 0,
+  kErrBounds = 1 << 1,   // a store outside its buffer (bounds-checked builds only)
 };
+
+// Bounds-checked builds (-DVQ_CHECK_BOUNDS, a sanitizer stand-in): a store
+// whose element index i is not below the extent n of its buffer, which the
+// host passes from the sizes of the call, is skipped and kErrBounds is OR-ed
+// into the status word. Normal builds compile the check away.
+#ifdef VQ_CHECK_BOUNDS
+__device__ __forceinline__ bool in_bounds(size_t i, size_t n, int32_t* err) {
+  if (i < n) return true;
+  if (err) atomicOr(err, kErrBounds);
+  return false;
+}
+#else
+__device__ __forceinline__ bool in_bounds(size_t, size_t, int32_t*) { return true; }
+#endif
 
 // A wait on an mbarrier gives up after this many SM clock cycles (about a
 // second), records kErrWaitTimeout and lets the kernel wind down instead of

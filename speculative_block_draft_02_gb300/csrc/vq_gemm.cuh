@@ -198,6 +198,10 @@ struct GemmParams {
   float* second;               // runner-up logit [M] (top-2 arg max), or null
   uint4* cand;                 // per-block (best, index, runner-up) [grid][M], or null
   int32_t* err;
+  // extents (elements) of the buffers the kernels store to, for the checks of
+  // bounds-checked builds: y, the split-K partials, the per-block arg max
+  // candidates
+  size_t y_elems, part_elems, cand_elems;
 };
 
 struct GemmLaunch {
@@ -395,6 +399,7 @@ __device__ __forceinline__ void top2_merge(float& v, uint32_t& n, bool& h, float
 __device__ __forceinline__ void argmax_decode(const GemmParams& p, int m, unsigned long long key,
                                               int nblocks) {
   const uint32_t n1 = key == 0ull ? 0xFFFFFFFFu : 0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull);
+  if (!in_bounds((size_t)m, (size_t)p.M, p.err)) return;
   if (key == 0ull) {
     p.argmax[m] = 0;
     if (p.maxval) p.maxval[m] = __uint_as_float(0x7FC00000u);
@@ -1404,7 +1409,8 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
               for (int e = 0; e < 4; ++e) {
                 const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
                 const int m = 8 * mt + 2 * t + (e & 1);
-                if (n < p.N && m < p.M) store_out<ACT>(p.y, (size_t)m * p.N + n, tot[r][mt][e]);
+                if (n < p.N && m < p.M && in_bounds((size_t)m * p.N + n, p.y_elems, p.err))
+                  store_out<ACT>(p.y, (size_t)m * p.N + n, tot[r][mt][e]);
               }
         }
       } else {
@@ -1420,7 +1426,9 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
               for (int e = 0; e < 4; ++e) {
                 const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
                 const int m = 8 * mt + 2 * t + (e & 1);
-                if (n < p.N && m < p.M) __stcg(part + (size_t)m * p.N + n, tot[r][mt][e]);
+                if (n < p.N && m < p.M &&
+                    in_bounds((size_t)sp * p.M * p.N + (size_t)m * p.N + n, p.part_elems, p.err))
+                  __stcg(part + (size_t)m * p.N + n, tot[r][mt][e]);
               }
         }
         __threadfence();
@@ -1481,7 +1489,8 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
                 for (int e = 0; e < 4; ++e) {
                   const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
                   const int m = 8 * mt + 2 * t + (e & 1);
-                  if (n < p.N && m < p.M) store_out<ACT>(p.y, (size_t)m * p.N + n, acc[r][mt][e]);
+                  if (n < p.N && m < p.M && in_bounds((size_t)m * p.N + n, p.y_elems, p.err))
+                    store_out<ACT>(p.y, (size_t)m * p.N + n, acc[r][mt][e]);
                 }
           }
           if (threadIdx.x == 0) p.cnt[rb] = 0u;
@@ -1552,9 +1561,9 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
       if (h && m < p.M && !aborted) {
         const unsigned long long key =
             ((unsigned long long)float_order(v) << 32) | (unsigned long long)(0xFFFFFFFFu - n);
-        atomicMax(p.keys + m, key);
+        if (in_bounds((size_t)m, (size_t)p.M, p.err)) atomicMax(p.keys + m, key);
       }
-      if (p.cand && m < p.M)
+      if (p.cand && m < p.M && in_bounds((size_t)blockIdx.x * p.M + m, p.cand_elems, p.err))
         p.cand[(size_t)blockIdx.x * p.M + m] =
             make_uint4(__float_as_uint(v), (h && !aborted) ? n : 0xFFFFFFFFu,
                        __float_as_uint(sv), 0u);

@@ -75,7 +75,8 @@ __global__ void kv_compact_kernel(KvTensors tp, int B, int H, int S_cap, int vec
                                   const int32_t* __restrict__ prefix_len,
                                   const int32_t* __restrict__ src_off,
                                   const int32_t* __restrict__ keep, int max_keep,
-                                  int32_t* __restrict__ new_len, int32_t* __restrict__ status) {
+                                  int32_t* __restrict__ new_len, int32_t* __restrict__ status,
+                                  int32_t* __restrict__ err) {
   extern __shared__ uint4 kv_buf[];
   const int h = blockIdx.x % H;
   const int b = (blockIdx.x / H) % B;
@@ -91,9 +92,14 @@ __global__ void kv_compact_kernel(KvTensors tp, int B, int H, int S_cap, int vec
   const int n = c * vec_per_slot;
   const uint4* src = row + (size_t)s * vec_per_slot;
   uint4* dst = row + (size_t)p * vec_per_slot;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) kv_buf[i] = src[i];
+  // Bounds-checked builds test each vector index against the tensor's B*H*S_cap slots.
+  const size_t base = ((size_t)b * H + h) * (size_t)S_cap * vec_per_slot;
+  const size_t extent = (size_t)B * H * (size_t)S_cap * vec_per_slot;
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    if (in_bounds(base + (size_t)s * vec_per_slot + i, extent, err)) kv_buf[i] = src[i];
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = kv_buf[i];
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    if (in_bounds(base + (size_t)p * vec_per_slot + i, extent, err)) dst[i] = kv_buf[i];
 }
 
 }  // namespace vq
@@ -150,9 +156,11 @@ extern "C" int kv_compact_per_row(void* const* tensors, int n_tensors, int B, in
   const long long blocks = (long long)n_tensors * B * H;
   const size_t smem = (size_t)(buf_bytes > 0 ? buf_bytes : 16);
   if (smem > 48 * 1024 && ensure_smem<kv_compact_kernel>(smem) != VQ_OK) return VQ_ECUDA;
+  int32_t* err = nullptr;
+  if (device_error_word(&err) != VQ_OK) return VQ_ECUDA;
   kv_compact_kernel<<<(unsigned)blocks, 256, smem, (cudaStream_t)stream>>>(
       tp, B, H, S_cap, (int)(slot_bytes / 16), prefix_len, src_off, keep, max_keep, new_len,
-      status);
+      status, err);
   return cudaGetLastError() == cudaSuccess ? VQ_OK : VQ_ECUDA;
 }
 

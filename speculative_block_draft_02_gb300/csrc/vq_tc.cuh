@@ -669,7 +669,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int i = 0; i < HC; ++i) {
             const int m = HC * ch + i;
-            if (m < p.M) store_out<ACT>(p.y, (size_t)m * p.N + n, tot[i]);
+            if (m < p.M && in_bounds((size_t)m * p.N + n, p.y_elems, p.err))
+              store_out<ACT>(p.y, (size_t)m * p.N + n, tot[i]);
           }
         }
       } else {
@@ -708,9 +709,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (vh && ft < p.M && !aborted) {
           const unsigned long long key =
               ((unsigned long long)float_order(v) << 32) | (unsigned long long)(0xFFFFFFFFu - vn);
-          atomicMax(p.keys + ft, key);
+          if (in_bounds((size_t)ft, (size_t)p.M, p.err)) atomicMax(p.keys + ft, key);
         }
-        if (p.cand && ft < p.M)
+        if (p.cand && ft < p.M && in_bounds((size_t)blockIdx.x * p.M + ft, p.cand_elems, p.err))
           p.cand[(size_t)blockIdx.x * p.M + ft] =
               make_uint4(__float_as_uint(v), (vh && !aborted) ? vn : 0xFFFFFFFFu,
                          __float_as_uint(vs), 0u);
