@@ -564,7 +564,7 @@ def run_vocab(args):
 def attention_bytes(case):
     """Algorithmic HBM bytes of one verify_attention call: the prefix keys and
     values it reads, the block's q, k, v, the appended cache slots and the output
-    (the per-chunk partial results stay in L2 and are not counted)."""
+    (the partial results stay in the clusters' shared memory)."""
     B, L, Hq, D = case.q.shape
     Hkv = case.k_new.shape[2]
     prefix = int(np.asarray(case.prefix_len, dtype=np.int64).sum()) * Hkv * D * 2 * 2
@@ -636,10 +636,9 @@ def run_attn(args):
                                                  ATTENTION_UNITS),
                      "algorithmic_bytes": nbytes, "flops": attention_flops(case),
                      "tflops": attention_flops(case) / per_call / 1e12,
-                     "kernel": "verify_attn_rope_kernel + verify_attn_partial_kernel + "
-                               "verify_attn_combine_kernel (time per call, all three launches)",
+                     "kernel": "verify_attn_kernel (one cluster launch per call)",
                      "us_per_launch": per_call * 1e6},
-        "gpu_launches": 3 * K_steps, "clocks": clk,
+        "gpu_launches": K_steps, "clocks": clk,
     }
     if rank == 0 and not args.no_cpu:
         import oracle

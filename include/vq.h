@@ -355,14 +355,16 @@ int verify_round_multi(const void* h, int B, int L, int K, int N, const uint32_t
  * status        optional int32 on the device: a row with P < 0, S < P or
  *               S + L > S_cap is left untouched in the caches, gets zero
  *               output, and bit 0 is OR-ed into *status (never cleared).
- * workspace     verify_attention_workspace_bytes(...) bytes, 16-byte aligned;
- *               no initial contents needed.
+ * workspace     not used (verify_attention_workspace_bytes returns 0 for
+ *               every shape); any pointer and size, null and 0 included.
  * Sizes         B >= 1, 1 <= L <= 64, Hq a multiple of Hkv, D 64 or 128
  *               (VQ_EUNSUPPORTED otherwise), L <= S_cap <= 2^24, rotary_dim
  *               even in 0..D, theta > 0 when rotary_dim > 0.
- * Three kernels: one rotating the block's queries into the workspace and its
- * keys into the cache (and appending its values), one per (chunk of 64 keys,
- * KV head, group of 64 query rows, batch row), and one that merges the chunks.
+ * One kernel, in clusters of 8 blocks: a cluster per (batch row, KV head,
+ * group of 64 query rows). Each block rotates the group's queries, takes
+ * every 8th chunk of 64 keys with an online softmax, and the cluster merges
+ * its blocks' partial results through distributed shared memory; the
+ * clusters of the first query group also append the block to the caches.
  */
 size_t verify_attention_workspace_bytes(int B, int L, int Hq, int Hkv, int D, int S_cap);
 int verify_attention(const void* q, const void* k_new, const void* v_new, void* k_cache,

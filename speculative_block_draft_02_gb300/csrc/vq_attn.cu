@@ -6,28 +6,33 @@
 // own logical positions, and no query sees the stale gap between its row's
 // valid prefix and the verify slots the rectangular cache shares across rows.
 //
-// Three kernels per call:
-//   verify_attn_rope_kernel  one block per (block position j, batch row): the
-//       (cos, sin) of the row's logical position P + j once, then the position's
-//       queries rotated and rounded to the storage type into the workspace, its
-//       keys rotated into cache slot S + j and its values copied to slot S + j.
-//   verify_attn_partial_kernel  one block per (key chunk of 64, KV head, group
-//       of 64 query rows, batch row). It stages the group's rotated queries and
-//       the chunk's keys and values (prefix slots, then the block's slots) in
-//       shared memory, every load requested before any is waited for, then four
-//       warps of 16 query rows each run S = Q K^T and O = P V on mma.sync
-//       m16n8k16 with the softmax in fp32. For bf16, P is split into a 16-bit
-//       high part and a 16-bit remainder so that the probabilities keep about
-//       16 significant bits through the tensor cores. It writes the chunk's
-//       unnormalised output and its (max, sum) per row to the workspace.
-//   verify_attn_combine_kernel  merges the chunks of every query row and writes
-//       the 16-bit output.
-// 52 KB of shared memory and at most 128 registers a thread let four partial
-// blocks share an SM. The partial and the merge kernels are launched with
-// programmatic stream serialization: each may be scheduled while the kernel
-// before it runs and waits for it (griddepcontrol.wait) before reading what it
-// wrote; the partial kernel requests the prefix keys and values, which the
-// rotation kernel does not write, before that wait.
+// One kernel per call, launched in clusters of kCluster blocks: one cluster per
+// (batch row b, KV head hk, group of 64 query rows). Query row rr of a group is
+// (block position j, query head hq) with rr = j * G + (hq - hk * G).
+//   - Logical key t of the row is cache slot t below P and the block's key
+//     t - P from P on (slot S + t - P once appended). Block r of the cluster
+//     takes the row's chunks of 64 keys r, r + kCluster, ...: the prefix rows
+//     of a chunk arrive as 2-D TMA boxes in a two-deep ring, both stages
+//     requested before anything else is done. The block's keys span at most
+//     two consecutive chunks, so each block owns at most one of them: it
+//     prefetches those rows of k_new and v_new at the start (up to 16 of
+//     them; more are loaded when the chunk comes), places them in
+//     the chunk's tile, rotates the keys at P + j there and, in row group 0,
+//     appends keys and values to slots S + j of the caches.
+//   - Meanwhile the block loads the group's queries, rotates them at P + j and
+//     rounds them to the storage type (the (cos, sin) of up to 16 positions at
+//     a time in a shared table, the frequencies staged in shared memory).
+//   - Four warps of 16 query rows run S = Q K^T and O = P V on mma.sync
+//     m16n8k16 over each chunk, with an online softmax in fp32. For bf16, P is
+//     split into a 16-bit high part and the remainder, so that the
+//     probabilities keep about 16 significant bits through the tensor cores.
+//   - Each block leaves its (max, sum, unnormalised output) per query row in
+//     its shared memory. After a cluster barrier, block r merges rows
+//     8r .. 8r + 7 over the cluster's blocks in rank order (a fixed order),
+//     reading its peers' shared memory, and writes the 16-bit output; a second
+//     cluster barrier keeps every block resident until its peers have read it.
+// No workspace. The launch is ordered after everything before it in the
+// stream (the caches' prefixes may have been written just before).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -39,14 +44,16 @@ namespace vq {
 namespace {
 
 constexpr int kAttnThreads = 128;  // four warps of 16 query rows
-constexpr int kAttnRows = 64;      // query rows per block
-constexpr int kChunk = 64;         // keys per block (two threads per key when staging V)
+constexpr int kAttnRows = 64;      // query rows per cluster
+constexpr int kChunk = 64;         // keys per chunk
+constexpr int kCluster = 8;        // blocks per cluster (portable size)
+constexpr int kMergeRows = kAttnRows / kCluster;
+constexpr int kAppRows = 16;       // block rows a block prefetches for its boundary chunk
 constexpr int kMaxRotPairs = 64;   // rotary_dim / 2 for D <= 128
+constexpr int kTabPos = 16;        // positions per (cos, sin) table pass
 constexpr int kMaxBlock = 64;      // largest verify block L
 constexpr int kMaxCap = 1 << 24;   // positions stay exact in fp32
-
-constexpr int kRopeThreads = 256;
-static_assert(kAttnThreads == 2 * kChunk, "the value tile is staged two threads per key");
+static_assert(kMergeRows * 16 == kAttnThreads, "sixteen threads per merged row");
 static_assert(kChunk == 8 * 8, "the score tile is eight mma n-tiles of 8 keys");
 
 struct AttnParams {
@@ -59,13 +66,10 @@ struct AttnParams {
   const int32_t* src_off;
   uint16_t* out;
   int32_t* status;
-  int32_t* err;     // the library's status word (a wait that gave up)
-  float* part_o;    // [B][Hkv][RG][NC][64][D]   unnormalised chunk outputs
-  float2* part_ml;  // [B][Hkv][RG][NC][64]      (max in log2 units, sum)
-  uint16_t* q_rot;  // [B][Hkv][RG][64][D] rotated, rounded queries, one swizzled tile
-                    // per (row, KV head, group of 64 query rows) (sw_off layout)
-  size_t cache_elems, out_elems, part_rows, qrot_bytes;   // extents (bounds-checked builds)
-  int L, Hq, Hkv, G, R, RG, NC, S_cap, rot_half;
+  int32_t* err;                      // the library's status word (a wait that gave up)
+  size_t cache_elems, out_elems;     // extents (bounds-checked builds)
+  int L, Hq, Hkv, G, R, RG, S_cap, rot_half;
+  int out_vec;                       // out is 16-byte aligned: vector stores
   float scale_log2;                  // scale * log2(e)
   float2 inv_freq[kMaxRotPairs];     // (hi, lo): hi + lo = theta^(-2i / rotary_dim)
 };
@@ -97,20 +101,90 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint3
   lo = (uint32_t)f2h<kF16>(a - h2f<kF16>(ha)) | ((uint32_t)f2h<kF16>(b - h2f<kF16>(hb)) << 16);
 }
 
-// 16 bytes global -> shared (at a shared-space address) without a register
-// round trip; zeros when !valid (nothing is read then).
-__device__ __forceinline__ void cp_async_16s(uint32_t dst, const void* src, bool valid) {
+__device__ __forceinline__ void sts64f(uint32_t a, float x, float y) {
+  asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
+
+__device__ __forceinline__ float2 lds64f(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts16(uint32_t a, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a)
+               : "memory");
+  return v;
+}
+
+// 16 bytes global -> shared without a register round trip; zeros when !valid
+// (nothing is read then). Completed by cp_async_wait_all.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0)
                : "memory");
 }
 
-__device__ __forceinline__ void sts128_zero(uint32_t addr) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
-}
-
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy accesses of shared memory before later
+// async-proxy (TMA) writes to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every block of the cluster: shared-memory writes before it
+// are visible to the whole cluster after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The two halves of a cluster barrier: an arrival that orders nothing, and a
+// wait (with acquire) for every thread of the cluster to have arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The address of the same shared-memory location in block `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_peer_v4(uint32_t a, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_peer_f2(uint32_t a, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
 }
 
 // Byte offset of element (row, col) of a [64 rows][D] 16-bit tile kept as D/64
@@ -121,394 +195,571 @@ __device__ __forceinline__ uint32_t sw_off(int row, int col) {
   return (uint32_t)((col >> 6) * 8192 + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4));
 }
 
+// The same for any column (one 16-bit element).
+__device__ __forceinline__ uint32_t el_off(int row, int col) {
+  return sw_off(row, col & ~7) + (uint32_t)(col & 7) * 2u;
+}
+
 __device__ __forceinline__ bool row_in_range(int P, int S, int L, int S_cap) {
   return P >= 0 && S >= P && (long long)S + L <= (long long)S_cap;
 }
 
 // (cos, sin) of pos * f for f = hi + lo: the angle is formed as a + err with
 // a = fl(pos * hi) and err the rest of pos * (hi + lo), then turned to first
-// order: sin(a + err) ~ sin a + err cos a (|err| < 1e-3 rad).
+// order: sin(a + err) ~ sin a + err cos a (|err| < 1e-3 rad). Every rounding
+// is spelled out, so that the same position gives the same bits everywhere.
 __device__ __forceinline__ float2 rope_cos_sin(float pos, float2 f) {
-  const float a = pos * f.x;
-  const float err = fmaf(pos, f.x, -a) + pos * f.y;
+  const float a = __fmul_rn(pos, f.x);
+  const float err = __fadd_rn(__fmaf_rn(pos, f.x, -a), __fmul_rn(pos, f.y));
   float s, c;
   sincosf(a, &s, &c);
-  return make_float2(c - err * s, s + err * c);
+  return make_float2(__fmaf_rn(-err, s, c), __fmaf_rn(err, c, s));
 }
 
-// One block per (block position j, batch row). Rows of the position: the Hq
-// query heads (rotated into the workspace), the Hkv key heads (rotated into
-// cache slot S + j) and the Hkv value heads (copied to slot S + j); dimensions
-// past rotary_dim are copied unchanged. Up to 64 rows at a time go through
-// shared memory: all of their 16-byte loads are requested together, the
-// pairs are turned in place, then the rows are stored in 16-byte pieces.
-template <bool kF16, int D>
-__global__ void __launch_bounds__(kRopeThreads)
-    verify_attn_rope_kernel(const __grid_constant__ AttnParams p) {
-  constexpr int RP = 64;       // rows per pass
-  constexpr int DC = D / 8;    // 16-byte pieces per row
-  __shared__ float2 cs[kMaxRotPairs];
-  __shared__ __align__(16) uint16_t tile[RP * D];
-  grid_launch_dependents();    // the partial kernel may be scheduled; it waits for this one
-  const int j = blockIdx.x, b = blockIdx.y;
-  const int P = p.prefix_len[b], S = p.src_off[b];
-  if (!row_in_range(P, S, p.L, p.S_cap)) return;   // flagged by the combine kernel
-  const int rh = p.rot_half;
-  const int tid = threadIdx.x;
-  // row r of the position: where it comes from and where it goes
-  auto row_src = [&](int r) -> const uint16_t* {
-    if (r < p.Hq) return p.q + (((size_t)b * p.L + j) * p.Hq + r) * D;
-    if (r < p.Hq + p.Hkv) return p.k_new + (((size_t)b * p.L + j) * p.Hkv + (r - p.Hq)) * D;
-    return p.v_new + (((size_t)b * p.L + j) * p.Hkv + (r - p.Hq - p.Hkv)) * D;
-  };
-  // key and value rows go to cache slot S + j; query head hq to row
-  // rr = j * G + (hq - hk * G) of its group's tile
-  auto row_dst = [&](int r) -> uint16_t* {
-    const int h = r < p.Hq + p.Hkv ? r - p.Hq : r - p.Hq - p.Hkv;
-    uint16_t* cache = r < p.Hq + p.Hkv ? p.k_cache : p.v_cache;
-    return cache + (((size_t)b * p.Hkv + h) * p.S_cap + (S + j)) * D;
-  };
-  const int rows = p.Hq + 2 * p.Hkv, n_rot = p.Hq + p.Hkv;
-  for (int r0 = 0; r0 < rows; r0 += RP) {
-    const int nr = min(RP, rows - r0);
-    if (r0 > 0) __syncthreads();   // the previous pass has stored its rows
-#pragma unroll 4
-    for (int i = tid; i < nr * DC; i += kRopeThreads) {
-      const int rl = i / DC, c = i - rl * DC;
-      *reinterpret_cast<uint4*>(tile + rl * D + c * 8) =
-          __ldg(reinterpret_cast<const uint4*>(row_src(r0 + rl)) + c);
-    }
-    // the angles of the position, while the first rows are in flight
-    if (r0 == 0)
-      for (int e = tid; e < rh; e += kRopeThreads) cs[e] = rope_cos_sin((float)(P + j), p.inv_freq[e]);
-    __syncthreads();
-    const int nrot = max(0, min(nr, n_rot - r0));   // rows of this pass that turn
-    for (int i = tid; i < nrot * rh; i += kRopeThreads) {
-      const int rl = i / rh, e = i - rl * rh;
-      uint16_t* row = tile + rl * D;
-      const float x1 = h2f<kF16>(row[e]), x2 = h2f<kF16>(row[e + rh]);
-      row[e] = f2h<kF16>(x1 * cs[e].x - x2 * cs[e].y);
-      row[e + rh] = f2h<kF16>(x2 * cs[e].x + x1 * cs[e].y);
-    }
-    __syncthreads();
-    for (int i = tid; i < nr * DC; i += kRopeThreads) {
-      const int rl = i / DC, c = i - rl * DC;
-      const int r = r0 + rl;
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + rl * D + c * 8);
-      if (r < p.Hq) {
-        const int hk = r / p.G, rr = j * p.G + (r - hk * p.G);
-        const int rg = rr / kAttnRows, row = rr - rg * kAttnRows;
-        const size_t off = (((size_t)b * p.Hkv + hk) * p.RG + rg) * (size_t)(kAttnRows * D * 2) +
-                           sw_off(row, c * 8);
-        if (in_bounds(off, p.qrot_bytes, p.err))
-          *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.q_rot) + off) = v;
-      } else {
-        uint16_t* d = row_dst(r) + c * 8;
-        if (in_bounds((size_t)(d - (r < p.Hq + p.Hkv ? p.k_cache : p.v_cache)), p.cache_elems, p.err))
-          *reinterpret_cast<uint4*>(d) = v;
-      }
-    }
+// The pair (x1, x2) turned by the angle of cs = (cos, sin), each result with
+// one rounded product and one fused multiply-add, spelled out so that every
+// place that rotates a key gets the same bits.
+__device__ __forceinline__ void rot_pair(float x1, float x2, float2 cs, float& r1, float& r2) {
+  r1 = __fmaf_rn(x1, cs.x, -__fmul_rn(x2, cs.y));
+  r2 = __fmaf_rn(x2, cs.x, __fmul_rn(x1, cs.y));
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Eight consecutive pairs of a row: dimensions e0 .. e0 + 7 (16 bytes at
+// shared address a1) with their partners e0 + rh .. (16 bytes at a2), turned
+// by cs[k] = (cos, sin) of pair e0 + k and rounded to the storage type in place.
+// Two 16-bit values (low, high) as floats, and two floats rounded into one word.
+template <bool kF16>
+__device__ __forceinline__ float2 h2f2(uint32_t w) {
+  if constexpr (kF16) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  } else {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
   }
 }
 
-// A bounded wait on phase 0 of an mbarrier: false after about a second.
-__device__ __forceinline__ bool attn_wait(uint32_t bar) {
-  if (mbar_try_wait(bar, 0u)) return true;
+template <bool kF16>
+__device__ __forceinline__ uint32_t f2h2(float lo, float hi) {
+  if constexpr (kF16) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  } else {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+  }
+}
+
+// Eight consecutive pairs of a row: dimensions e0 .. e0 + 7 (16 bytes at
+// shared address a1) with their partners e0 + rh .. (16 bytes at a2), turned
+// by cs[k] = (cos, sin) of pair e0 + k and rounded to the storage type in place.
+template <bool kF16>
+__device__ __forceinline__ void rot8(uint32_t a1, uint32_t a2, const float2 (&cs)[8]) {
+  const uint4 x1 = lds128(a1), x2 = lds128(a2);
+  const uint32_t w1[4] = {x1.x, x1.y, x1.z, x1.w}, w2[4] = {x2.x, x2.y, x2.z, x2.w};
+  uint32_t o1[4], o2[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 u = h2f2<kF16>(w1[k]), v = h2f2<kF16>(w2[k]);
+    float r1a, r2a, r1b, r2b;
+    rot_pair(u.x, v.x, cs[2 * k], r1a, r2a);
+    rot_pair(u.y, v.y, cs[2 * k + 1], r1b, r2b);
+    o1[k] = f2h2<kF16>(r1a, r1b);
+    o2[k] = f2h2<kF16>(r2a, r2b);
+  }
+  sts128(a1, make_uint4(o1[0], o1[1], o1[2], o1[3]));
+  sts128(a2, make_uint4(o2[0], o2[1], o2[2], o2[3]));
+}
+
+// A bounded wait on an mbarrier phase: false after about a second.
+__device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, 0u))
+  while (!mbar_try_wait(bar, parity))
     if (clock64() - t0 > kWaitTimeoutCycles) return false;
   return true;
 }
 
-template <bool kF16, int D>
-__global__ void __launch_bounds__(kAttnThreads, 4)
-    verify_attn_partial_kernel(const __grid_constant__ CUtensorMap tm_k,
-                               const __grid_constant__ CUtensorMap tm_v,
-                               const __grid_constant__ AttnParams p) {
-  constexpr uint32_t TILE = kAttnRows * D * 2;   // bytes of a 64-row tile
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t Qs = (raw + 1023u) & ~1023u;   // the swizzle wants 1 KiB-aligned tiles
-  const uint32_t Ks = Qs + TILE, Vs = Qs + 2 * TILE;
-  const uint32_t bar_pre = Qs + 3 * TILE, bar_rest = bar_pre + 8u;
+// Shared memory of a block (offsets from a 1 KiB-aligned base; TILE = 64 rows
+// of D 16-bit values): the rotated queries, then the ring's two stages of
+// (keys, values), the (cos, sin) table of the prefetched block keys, those
+// block rows of this block's boundary chunk (keys, then values, as given),
+// the rotation frequencies, the (cos, sin) table of this block's query rows'
+// positions and two mbarriers. After the last chunk the
+// ring holds the block's partial results: the unnormalised outputs
+// [64][D + 4] fp32 (rows padded against bank conflicts), then (max, sum) [64].
+template <int D>
+struct AttnSmem {
+  static constexpr uint32_t TILE = kAttnRows * D * 2;
+  static constexpr uint32_t Q = 0, RING = TILE, TAB = 5 * TILE;
+  static constexpr uint32_t APP = TAB + kTabPos * kMaxRotPairs * 8;
+  static constexpr uint32_t FREQ = APP + 2 * kAppRows * D * 2;
+  static constexpr uint32_t TABQ = FREQ + kMaxRotPairs * 8;
+  static constexpr uint32_t BARS = TABQ + kMergeRows * kMaxRotPairs * 8;
+  static constexpr uint32_t BYTES = BARS + 16;
+  static constexpr uint32_t O_STRIDE = (D + 4) * 4;
+  static constexpr uint32_t OM = RING, ML = RING + kAttnRows * O_STRIDE;
+  static_assert(kAttnRows * O_STRIDE + kAttnRows * 8 <= 4 * TILE, "partials fit in the ring");
+};
 
-  const int chunk = blockIdx.x;
-  const int hk = blockIdx.y / p.RG, rg = blockIdx.y % p.RG;
-  const int b = blockIdx.z;
-  const int P = p.prefix_len[b], S = p.src_off[b];
-  if (!row_in_range(P, S, p.L, p.S_cap)) return;   // flagged by the combine kernel
-  const int T = P + p.L;                            // visible keys of the last query
-  const int c0 = chunk * kChunk;
-  if (c0 >= T) return;
+template <bool kF16, int D>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads, 2)
+    verify_attn_kernel(const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ AttnParams p) {
+  using SM = AttnSmem<D>;
+  constexpr uint32_t TILE = SM::TILE;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;   // the swizzle wants 1 KiB
+  const uint32_t Qs = base + SM::Q, tab = base + SM::TAB, app = base + SM::APP;
+  const uint32_t freq = base + SM::FREQ, tabq = base + SM::TABQ, bars = base + SM::BARS;
+
   const int tid = threadIdx.x;
-  grid_launch_dependents();   // the merge may be scheduled; it waits for this kernel
+  const uint32_t rank = cluster_rank();
+  const int hk = blockIdx.y / p.RG, rg = blockIdx.y - hk * p.RG;
+  const int b = blockIdx.z;
+  const int rr0 = rg * kAttnRows;
+  const int P = p.prefix_len[b], S = p.src_off[b];
+  if (!row_in_range(P, S, p.L, p.S_cap)) {
+    // the whole cluster leaves here (no barrier follows): zero output, flagged
+    for (int i = tid; i < kMergeRows * D; i += kAttnThreads) {
+      const int rr = rr0 + (int)rank * kMergeRows + i / D, d = i % D;
+      if (rr < p.R) {
+        const int j = rr / p.G, hq = hk * p.G + (rr - j * p.G);
+        const size_t o = (((size_t)b * p.L + j) * p.Hq + hq) * D + d;
+        if (in_bounds(o, p.out_elems, p.err)) p.out[o] = 0;
+      }
+    }
+    if (rank == 0 && blockIdx.y == 0 && tid == 0 && p.status) atomicOr(p.status, 1);
+    return;
+  }
+  const int T = P + p.L;   // visible keys of the last query
+  const int n_chunks = (T + kChunk - 1) / kChunk;
+  const int n_mine = (int)rank < n_chunks ? (n_chunks - 1 - (int)rank) / kCluster + 1 : 0;
+  const size_t head = ((size_t)b * p.Hkv + hk) * p.S_cap;   // cache row of slot 0
+  const int rh = p.rot_half;
+
   if (tid == 0) {
-    mbar_init(bar_pre, 1);
-    mbar_init(bar_rest, 1);
+    mbar_init(bars, 1);
+    mbar_init(bars + 8, 1);
     fence_mbar_init();
   }
   __syncthreads();
-
-  // Key tl of the chunk (t = c0 + tl) sits in cache slot t below P and in slot
-  // S + (t - P) from P on. The chunk's rows from slot c0 on arrive as 2-D TMA
-  // boxes of 64 rows x 64 values (two per tile at D = 128), requested before
-  // the wait for the rotation kernel (which writes only slots S.. and the
-  // rotated queries; everything before it in the stream had completed when it
-  // started); that is the whole chunk when it lies in the prefix. In a chunk
-  // that reaches the block, the rows from P on are then replaced, once the
-  // boxes have landed: the block's keys and values (slots S..) 16 bytes at a
-  // time into the same swizzled layout, zeros past T. The group's rotated
-  // queries are one tile of the workspace: one bulk copy after the wait.
-  const bool whole = c0 + kChunk <= P;
-  const int n_pre = max(0, min(P - c0, kChunk));   // prefix rows: tl < n_pre
-  const int n_vis = min(T - c0, kChunk);           // visible rows: tl < n_vis
-  const size_t head = ((size_t)b * p.Hkv + hk) * p.S_cap;
-  if (tid == 0) {
-    if (n_pre > 0) {
-      mbar_arrive_expect_tx(bar_pre, 2u * TILE);
+  // thread 0: the prefix rows of chunk i of this block into stage i % 2 (the
+  // whole box; rows from P on are replaced once it has landed)
+  auto issue = [&](int i) {
+    const int c0 = ((int)rank + i * kCluster) * kChunk;
+    const uint32_t bar = bars + 8u * (uint32_t)(i & 1);
+    const uint32_t Ks = base + SM::RING + (uint32_t)(i & 1) * 2u * TILE, Vs = Ks + TILE;
+    if (c0 < P) {
+      mbar_arrive_expect_tx(bar, 2u * TILE);
 #pragma unroll
       for (int sg = 0; sg < D / 64; ++sg) {
-        tma_load_2d(Ks + sg * 8192, &tm_k, sg * 64, (int)(head + c0), bar_pre);
-        tma_load_2d(Vs + sg * 8192, &tm_v, sg * 64, (int)(head + c0), bar_pre);
+        tma_load_2d(Ks + sg * 8192, &tm_k, sg * 64, (int)(head + c0), bar);
+        tma_load_2d(Vs + sg * 8192, &tm_v, sg * 64, (int)(head + c0), bar);
       }
     } else {
-      mbar_arrive(bar_pre);
+      mbar_arrive(bar);
     }
-  }
-  grid_wait_prerequisites();
+  };
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar_rest, TILE);
-    bulk_load(Qs,
-              reinterpret_cast<const uint8_t*>(p.q_rot) +
-                  (((size_t)b * p.Hkv + hk) * p.RG + rg) * (size_t)TILE,
-              TILE, bar_rest);
+    if (n_mine > 0) issue(0);
+    if (n_mine > 1) issue(1);
   }
-  bool ok = true;
-  if (!whole) {
-    ok = attn_wait(bar_pre);   // the boxes' rows past n_pre are replaced next
-    if (ok) {
-      for (int i = tid; i < (n_vis - n_pre) * (D / 8); i += kAttnThreads) {
-        const int tl = n_pre + i / (D / 8), c = i % (D / 8);
-        const size_t slot = head + (size_t)(S + (c0 + tl - P));
-        const uint32_t o = sw_off(tl, c * 8);
-        const bool in = in_bounds(slot * D + c * 8, p.cache_elems, p.err);
-        cp_async_16s(Ks + o, p.k_cache + (in ? slot * D + c * 8 : 0), in);
-        cp_async_16s(Vs + o, p.v_cache + (in ? slot * D + c * 8 : 0), in);
-      }
-      for (int i = tid; i < (kChunk - n_vis) * (D / 8); i += kAttnThreads) {
-        const int tl = n_vis + i / (D / 8), c = i % (D / 8);
-        const uint32_t o = sw_off(tl, c * 8);
-        sts128_zero(Ks + o);
-        sts128_zero(Vs + o);
-      }
-      cp_async_wait_all();
+
+  // every block of the cluster has started once this barrier completes (before
+  // the first write into a peer's shared memory)
+  cluster_arrive_relaxed();
+  // this block's eight query rows of the group (zeros past R)
+  const int q0 = (int)rank * kMergeRows;   // local rows q0 .. q0 + 7
+  for (int i = tid; i < kMergeRows * (D / 8); i += kAttnThreads) {
+    const int lr = q0 + i / (D / 8), c = i % (D / 8);
+    const int rr = rr0 + lr;
+    const bool valid = rr < p.R;
+    const int j = valid ? rr / p.G : 0, hq = valid ? hk * p.G + (rr - j * p.G) : 0;
+    cp_async_16(Qs + sw_off(lr, c * 8), p.q + (((size_t)b * p.L + j) * p.Hq + hq) * D + c * 8,
+                valid);
+  }
+  // the block rows jb0 .. jb1 - 1 of this block's boundary chunk (the block
+  // keys span at most two consecutive chunks, so a block owns at most one),
+  // prefetched when they fit
+  int jb0 = 0, jb1 = 0;
+  for (int ci = P / kChunk; ci * kChunk < T; ++ci)
+    if (ci % kCluster == (int)rank) {
+      jb0 = max(ci * kChunk, P) - P;
+      jb1 = min(ci * kChunk + kChunk, T) - P;
+    }
+  const bool staged = jb1 - jb0 <= kAppRows;
+  if (staged)
+    for (int i = tid; i < (jb1 - jb0) * 2 * (D / 8); i += kAttnThreads) {
+      const int a = i / (2 * (D / 8)), rem = i - a * (2 * (D / 8));
+      const int kv = rem / (D / 8), c = rem - kv * (D / 8);
+      cp_async_16(app + (uint32_t)((kv * kAppRows + a) * D * 2 + c * 16),
+                  (kv ? p.v_new : p.k_new) + (((size_t)b * p.L + jb0 + a) * p.Hkv + hk) * D + c * 8,
+                  true);
+    }
+  // while the copies land: the frequencies into shared memory, the (cos, sin)
+  // of this block's query positions P + jq0 .. (at most eight) and of the
+  // prefetched keys' positions P + jb0 ..; each thread keeps one frequency
+  // (one read of the parameter array each)
+  const bool vec8 = (rh & 7) == 0;
+  const int npc = vec8 ? rh / 8 : rh;   // rotation steps per row
+  const int tab_lo = jb0, tab_n = staged ? jb1 - jb0 : 0;
+  const int q_end = min(p.R, rr0 + q0 + kMergeRows);   // this block's query rows: .. q_end - 1
+  const int jq0 = (rr0 + q0) / p.G, nq = q_end > rr0 + q0 ? (q_end - 1) / p.G - jq0 + 1 : 0;
+  const int tpe = rh > 0 ? kAttnThreads / rh : 0;   // threads per frequency (rh <= 64)
+  if (tid < tpe * rh) {
+    const int e = tid % rh, j0 = tid / rh;
+    const float2 fq = p.inv_freq[e];
+    if (j0 == 0) sts64f(freq + (uint32_t)e * 8u, fq.x, fq.y);
+    for (int jj = j0; jj < nq; jj += tpe) {
+      const float2 cs = rope_cos_sin((float)(P + jq0 + jj), fq);
+      sts64f(tabq + (uint32_t)(jj * kMaxRotPairs + e) * 8u, cs.x, cs.y);
+    }
+    for (int jj = j0; jj < tab_n; jj += tpe) {
+      const float2 cs = rope_cos_sin((float)(P + tab_lo + jj), fq);
+      sts64f(tab + (uint32_t)(jj * kMaxRotPairs + e) * 8u, cs.x, cs.y);
     }
   }
-  if (!ok || !attn_wait(bar_pre) || !attn_wait(bar_rest)) {
-    // give up: report it, let the copies already issued land, and leave
-    if (tid == 0) atomicOr(p.err, kErrWaitTimeout);
-    attn_wait(bar_pre);
-    attn_wait(bar_rest);
-    return;
+  cp_async_wait_all();
+  __syncthreads();
+  // the eight rows rotated at P + j in place (eight pairs per step when rh is
+  // a multiple of 8, else one)
+  if (rh > 0)
+    for (int i = tid; i < (q_end - rr0 - q0) * npc; i += kAttnThreads) {
+      const int k = i / npc, u = i - k * npc;
+      const int lr = q0 + k;
+      const uint32_t cs_row = tabq + (uint32_t)(((rr0 + lr) / p.G - jq0) * kMaxRotPairs) * 8u;
+      if (vec8) {
+        float2 cs[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint4 w = lds128(cs_row + (uint32_t)(8 * u + 2 * m) * 8u);
+          cs[2 * m] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+          cs[2 * m + 1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+        }
+        rot8<kF16>(Qs + sw_off(lr, 8 * u), Qs + sw_off(lr, 8 * u + rh), cs);
+      } else {
+        const uint32_t a1 = Qs + el_off(lr, u), a2 = Qs + el_off(lr, u + rh);
+        float r1, r2;
+        rot_pair(h2f<kF16>(lds16(a1)), h2f<kF16>(lds16(a2)), lds64f(cs_row + (uint32_t)u * 8u), r1,
+                 r2);
+        sts16(a1, f2h<kF16>(r1));
+        sts16(a2, f2h<kF16>(r2));
+      }
+    }
+  __syncthreads();
+  // the eight rows into every other block's query tile (the same offsets)
+  cluster_wait();
+  for (int i = tid; i < (kCluster - 1) * kMergeRows * (D / 8); i += kAttnThreads) {
+    const int c = i % (D / 8), lr = q0 + (i / (D / 8)) % kMergeRows;
+    const uint32_t peer = ((uint32_t)(i / (kMergeRows * (D / 8))) + rank + 1u) % kCluster;
+    const uint32_t off = Qs + sw_off(lr, c * 8);
+    st_peer_v4(peer_addr(off, peer), lds128(off));
   }
-  __syncthreads();   // the gathered rows too
+  // (cos, sin) of pairs at block position j (position P + j): from the table
+  // when it holds the position (the same bits as computing it)
+  auto cs_one = [&](int j, int e) -> float2 {
+    const int jj = j - tab_lo;
+    if (jj >= 0 && jj < tab_n) return lds64f(tab + (uint32_t)(jj * kMaxRotPairs + e) * 8u);
+    return rope_cos_sin((float)(P + j), lds64f(freq + (uint32_t)e * 8u));
+  };
+  auto cs_eight = [&](int j, int e0, float2 (&cs)[8]) {
+    const int jj = j - tab_lo;
+    if (jj >= 0 && jj < tab_n) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 w = lds128(tab + (uint32_t)(jj * kMaxRotPairs + e0 + 2 * k) * 8u);
+        cs[2 * k] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+        cs[2 * k + 1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        cs[k] = rope_cos_sin((float)(P + j), lds64f(freq + (uint32_t)(e0 + k) * 8u));
+    }
+  };
+  // block key row at shared address row (16-bit values, dimension d at
+  // row_at(d)) of block position j: step u of its rotation
+  auto rot_key_step = [&](int j, int u, uint32_t a_lo, uint32_t a_hi) {
+    if (vec8) {
+      float2 cs[8];
+      cs_eight(j, 8 * u, cs);
+      rot8<kF16>(a_lo, a_hi, cs);
+    } else {
+      float r1, r2;
+      rot_pair(h2f<kF16>(lds16(a_lo)), h2f<kF16>(lds16(a_hi)), cs_one(j, u), r1, r2);
+      sts16(a_lo, f2h<kF16>(r1));
+      sts16(a_hi, f2h<kF16>(r2));
+    }
+  };
+
+  cluster_sync_all();   // every block's query tile is complete
 
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
   const int row0 = warp * 16;
-  const int rA = rg * kAttnRows + row0 + g, rB = rA + 8;   // rows of c0/c1 and c2/c3
-  if (rg * kAttnRows + row0 >= p.R) return;               // no barrier follows
-  const bool okA = rA < p.R, okB = rB < p.R;
-  const int jA = rA / p.G, jB = rB / p.G;
-
-  // S = Q K^T: A fragments of the warp's 16 query rows, B fragments of two
-  // 8-key tiles per ldmatrix.x4
-  float sc[8][4];
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+  const int rA = rr0 + row0 + g, rB = rA + 8;   // rows of c0/c1 and c2/c3
+  const bool live = rr0 + row0 < p.R;           // the warp has query rows
+  // the last visible key of each of the thread's two rows (-1: past R)
+  const int limA = rA < p.R ? P + rA / p.G : -1, limB = rB < p.R ? P + rB / p.G : -1;
   const int qa_row = row0 + (lane & 15), qa_col = (lane >> 4) * 8;
   const int kb_row = (lane & 7) + ((lane >> 4) << 3), kb_col = ((lane >> 3) & 1) * 8;
-#pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    uint32_t qa[4];
-    ldsm_x4(qa, Qs + sw_off(qa_row, ks * 16 + qa_col));
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      uint32_t kb[4];
-      ldsm_x4(kb, Ks + sw_off(np * 16 + kb_row, ks * 16 + kb_col));
-      mma_16816<kF16>(sc[2 * np], qa, kb[0], kb[1]);
-      mma_16816<kF16>(sc[2 * np + 1], qa, kb[2], kb[3]);
-    }
-  }
-  // mask (prefix for all, block keys causally, nothing past T), scale, row max;
-  // a chunk wholly in the prefix is visible to every row
-  float m[2] = {-INFINITY, -INFINITY};
-  if (c0 + kChunk <= P) {
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        sc[nt][e] *= p.scale_log2;
-        m[e >> 1] = fmaxf(m[e >> 1], sc[nt][e]);
-      }
-  } else {
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = c0 + nt * 8 + 2 * tq + (e & 1);
-        const int hh = e >> 1;
-        const bool vis = (hh ? okB : okA) && t < T && (t < P || t - P <= (hh ? jB : jA));
-        const float v = vis ? sc[nt][e] * p.scale_log2 : -INFINITY;
-        sc[nt][e] = v;
-        m[hh] = fmaxf(m[hh], v);
-      }
-    }
-  }
-  float mu[2], l[2] = {0.f, 0.f};
-#pragma unroll
-  for (int hh = 0; hh < 2; ++hh) {
-    m[hh] = fmaxf(m[hh], __shfl_xor_sync(0xffffffffu, m[hh], 1));
-    m[hh] = fmaxf(m[hh], __shfl_xor_sync(0xffffffffu, m[hh], 2));
-    mu[hh] = m[hh] == -INFINITY ? 0.f : m[hh];   // no visible key in the chunk: every p is 0
-  }
+  const int vb_row = (lane & 7) + ((lane >> 3) & 1) * 8, vb_col = (lane >> 4) * 8;
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
   float o[D / 8][4];
 #pragma unroll
   for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  // O = P V: P as 16-bit MMA operands. bf16 keeps 8 significant bits, which
-  // would move the outputs by up to 2^-9 relative, so there P is split into a
-  // high part and the remainder (two MMAs, about 16 bits); fp16's 11 bits
-  // suffice alone. B fragments of two 8-dimension tiles per ldmatrix.x4.trans.
-  const int vb_row = (lane & 7) + ((lane >> 3) & 1) * 8, vb_col = (lane >> 4) * 8;
-#pragma unroll
-  for (int kk = 0; kk < kChunk / 16; ++kk) {
-    uint32_t ah[4], al[4];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int nt = 2 * kk + half;
-      const float p0 = exp2f(sc[nt][0] - mu[0]), p1 = exp2f(sc[nt][1] - mu[0]);
-      const float p2 = exp2f(sc[nt][2] - mu[1]), p3 = exp2f(sc[nt][3] - mu[1]);
-      l[0] += p0 + p1;
-      l[1] += p2 + p3;
-      if constexpr (kF16) {
-        ah[2 * half] = (uint32_t)f2h<true>(p0) | ((uint32_t)f2h<true>(p1) << 16);
-        ah[2 * half + 1] = (uint32_t)f2h<true>(p2) | ((uint32_t)f2h<true>(p3) << 16);
-      } else {
-        split_pair<false>(p0, p1, ah[2 * half], al[2 * half]);
-        split_pair<false>(p2, p3, ah[2 * half + 1], al[2 * half + 1]);
-      }
-    }
-#pragma unroll
-    for (int np = 0; np < D / 16; ++np) {
-      uint32_t vb[4];
-      ldsm_x4_t(vb, Vs + sw_off(kk * 16 + vb_row, np * 16 + vb_col));
-      mma_16816<kF16>(o[2 * np], ah, vb[0], vb[1]);
-      mma_16816<kF16>(o[2 * np + 1], ah, vb[2], vb[3]);
-      if constexpr (!kF16) {
-        mma_16816<kF16>(o[2 * np], al, vb[0], vb[1]);
-        mma_16816<kF16>(o[2 * np + 1], al, vb[2], vb[3]);
-      }
-    }
-  }
-  for (int hh = 0; hh < 2; ++hh) {
-    l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 1);
-    l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 2);
-  }
-  const size_t part = (((size_t)b * p.Hkv + hk) * p.RG + rg) * p.NC + chunk;
-  float* po = p.part_o + part * kAttnRows * D;
-  float2* pml = p.part_ml + part * kAttnRows;
-  const int lA = row0 + g, lB = lA + 8;
-  const bool stA = okA && in_bounds(part * kAttnRows + lA, p.part_rows, p.err);
-  const bool stB = okB && in_bounds(part * kAttnRows + lB, p.part_rows, p.err);
-  if (stA) {
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
-      *reinterpret_cast<float2*>(po + lA * D + nd * 8 + 2 * tq) = make_float2(o[nd][0], o[nd][1]);
-    if (tq == 0) pml[lA] = make_float2(m[0], l[0]);
-  }
-  if (stB) {
-#pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd)
-      *reinterpret_cast<float2*>(po + lB * D + nd * 8 + 2 * tq) = make_float2(o[nd][2], o[nd][3]);
-    if (tq == 0) pml[lB] = make_float2(m[1], l[1]);
-  }
-}
 
-// One block per (block position j, query head, batch row), D threads. Lane l of
-// every warp covers dimensions VEC*l .. VEC*l + VEC-1; warp w takes chunks w,
-// w + NW, ... so that all of a row's chunks are requested at once; the warps'
-// sums are then added in warp order (a fixed order: the result does not depend
-// on timing).
-template <bool kF16, int D>
-__global__ void __launch_bounds__(D) verify_attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  constexpr int NW = D / 32, VEC = D / 32;
-  const int jh = blockIdx.x, b = blockIdx.y;
-  const int j = jh / p.Hq, hq = jh - j * p.Hq;
-  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  grid_wait_prerequisites();   // launched early (programmatic serialization)
-  const size_t dst_off = (((size_t)b * p.L + j) * p.Hq + hq) * D;
-  if (!in_bounds(dst_off + D - 1, p.out_elems, p.err)) return;
-  uint16_t* dst = p.out + dst_off;
-  const int P = p.prefix_len[b], S = p.src_off[b];
-  if (!row_in_range(P, S, p.L, p.S_cap)) {
-    dst[tid] = 0;
-    if (jh == 0 && tid == 0 && p.status) atomicOr(p.status, 1);
-    return;
+  bool ok = true;
+  int done = 0;   // chunks consumed
+  for (; done < n_mine; ++done) {
+    const int i = done;
+    const uint32_t Ks = base + SM::RING + (uint32_t)(i & 1) * 2u * TILE, Vs = Ks + TILE;
+    const int c0 = ((int)rank + i * kCluster) * kChunk;
+    const int n_pre = max(0, min(P - c0, kChunk));   // prefix rows: tl < n_pre
+    const int n_vis = min(T - c0, kChunk);           // visible rows: tl < n_vis
+    const bool got = attn_wait(bars + 8u * (uint32_t)(i & 1), (uint32_t)(i >> 1) & 1u);
+    if (c0 + kChunk > P) {
+      // the chunk reaches the block: its keys and values from P on (block rows
+      // jb0 ..), zeros past T; then the keys rotated, and row group 0 appends
+      // them with the values to slots S + jb0 ..
+      if (staged) {
+        for (int e = tid; e < (kChunk - n_pre) * (D / 8); e += kAttnThreads) {
+          const int tl = n_pre + e / (D / 8), c = e % (D / 8);
+          uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+          if (tl < n_vis) {
+            const int a = c0 + tl - P - jb0;
+            kv = lds128(app + (uint32_t)((a * D + c * 8) * 2));
+            vv = lds128(app + (uint32_t)(((kAppRows + a) * D + c * 8) * 2));
+          }
+          sts128(Ks + sw_off(tl, c * 8), kv);
+          sts128(Vs + sw_off(tl, c * 8), vv);
+        }
+      } else {
+        for (int e = tid; e < (kChunk - n_pre) * (D / 8); e += kAttnThreads) {
+          const int tl = n_pre + e / (D / 8), c = e % (D / 8);
+          const bool valid = tl < n_vis;
+          const size_t src =
+              valid ? (((size_t)b * p.L + (c0 + tl - P)) * p.Hkv + hk) * D + c * 8 : 0;
+          cp_async_16(Ks + sw_off(tl, c * 8), p.k_new + src, valid);
+          cp_async_16(Vs + sw_off(tl, c * 8), p.v_new + src, valid);
+        }
+        cp_async_wait_all();
+      }
+      __syncthreads();   // block-uniform branch: the rows are in place
+      if (rh > 0) {
+        for (int e = tid; e < (n_vis - n_pre) * npc; e += kAttnThreads) {
+          const int tl = n_pre + e / npc, u = e - (e / npc) * npc;
+          if (vec8)
+            rot_key_step(c0 + tl - P, u, Ks + sw_off(tl, 8 * u), Ks + sw_off(tl, 8 * u + rh));
+          else
+            rot_key_step(c0 + tl - P, u, Ks + el_off(tl, u), Ks + el_off(tl, u + rh));
+        }
+        __syncthreads();
+      }
+      if (rg == 0)
+        for (int e = tid; e < (n_vis - n_pre) * 2 * (D / 8); e += kAttnThreads) {
+          const int tl = n_pre + e / (2 * (D / 8)), rem = e % (2 * (D / 8));
+          const int kv = rem / (D / 8), c = rem - kv * (D / 8);
+          const uint4 v = lds128((kv ? Vs : Ks) + sw_off(tl, c * 8));
+          const size_t dst = (head + (size_t)(S + c0 + tl - P)) * D + c * 8;
+          if (in_bounds(dst + 7, p.cache_elems, p.err))
+            *reinterpret_cast<uint4*>((kv ? p.v_cache : p.k_cache) + dst) = v;
+        }
+    }
+    ok = __syncthreads_and(got) != 0;   // the whole tile, and one decision for the block
+    if (!ok) break;
+
+    if (live) {
+      // S = Q K^T: A fragments of the warp's 16 query rows, B fragments of two
+      // 8-key tiles per ldmatrix.x4
+      float sc[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t qa[4];
+        ldsm_x4(qa, Qs + sw_off(qa_row, ks * 16 + qa_col));
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          uint32_t kb[4];
+          ldsm_x4(kb, Ks + sw_off(np * 16 + kb_row, ks * 16 + kb_col));
+          mma_16816<kF16>(sc[2 * np], qa, kb[0], kb[1]);
+          mma_16816<kF16>(sc[2 * np + 1], qa, kb[2], kb[3]);
+        }
+      }
+      // mask, scale and the chunk's row maxima: key t is visible to query row
+      // (j) iff t <= P + j (the prefix, then the block causally; never past
+      // T); rows past R see nothing (lim -1)
+      float mc[2] = {-INFINITY, -INFINITY};
+      const int tb = c0 + 2 * tq;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int hh = e >> 1;
+          const float v =
+              tb + nt * 8 + (e & 1) <= (hh ? limB : limA) ? sc[nt][e] * p.scale_log2 : -INFINITY;
+          sc[nt][e] = v;
+          mc[hh] = fmaxf(mc[hh], v);
+        }
+      // online softmax: the running sums and outputs move to the new maximum
+      float mu[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        mc[hh] = fmaxf(mc[hh], __shfl_xor_sync(0xffffffffu, mc[hh], 1));
+        mc[hh] = fmaxf(mc[hh], __shfl_xor_sync(0xffffffffu, mc[hh], 2));
+        const float mn = fmaxf(m_run[hh], mc[hh]);
+        mu[hh] = mn == -INFINITY ? 0.f : mn;   // nothing visible yet: every p is 0
+        const float alpha = exp2f(m_run[hh] - mu[hh]);
+        m_run[hh] = mn;
+        l_run[hh] *= alpha;
+#pragma unroll
+        for (int nd = 0; nd < D / 8; ++nd) {
+          o[nd][2 * hh] *= alpha;
+          o[nd][2 * hh + 1] *= alpha;
+        }
+      }
+      // O += P V: P as 16-bit MMA operands (bf16: high part and remainder),
+      // B fragments of two 8-dimension tiles per ldmatrix.x4.trans
+#pragma unroll
+      for (int kk = 0; kk < kChunk / 16; ++kk) {
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int nt = 2 * kk + half;
+          const float p0 = exp2f(sc[nt][0] - mu[0]), p1 = exp2f(sc[nt][1] - mu[0]);
+          const float p2 = exp2f(sc[nt][2] - mu[1]), p3 = exp2f(sc[nt][3] - mu[1]);
+          l_run[0] += p0 + p1;
+          l_run[1] += p2 + p3;
+          if constexpr (kF16) {
+            ah[2 * half] = (uint32_t)f2h<true>(p0) | ((uint32_t)f2h<true>(p1) << 16);
+            ah[2 * half + 1] = (uint32_t)f2h<true>(p2) | ((uint32_t)f2h<true>(p3) << 16);
+          } else {
+            split_pair<false>(p0, p1, ah[2 * half], al[2 * half]);
+            split_pair<false>(p2, p3, ah[2 * half + 1], al[2 * half + 1]);
+          }
+        }
+#pragma unroll
+        for (int np = 0; np < D / 16; ++np) {
+          uint32_t vb[4];
+          ldsm_x4_t(vb, Vs + sw_off(kk * 16 + vb_row, np * 16 + vb_col));
+          mma_16816<kF16>(o[2 * np], ah, vb[0], vb[1]);
+          mma_16816<kF16>(o[2 * np + 1], ah, vb[2], vb[3]);
+          if constexpr (!kF16) {
+            mma_16816<kF16>(o[2 * np], al, vb[0], vb[1]);
+            mma_16816<kF16>(o[2 * np + 1], al, vb[2], vb[3]);
+          }
+        }
+      }
+    }
+    // this stage's reads and writes before the TMA reuses it (never after a
+    // chunk that reaches the block: that is the block's last)
+    if (i + 2 < n_mine) fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0 && i + 2 < n_mine) issue(i + 2);
   }
-  const int nc = (P + p.L + kChunk - 1) / kChunk;
-  const int hk = hq / p.G, rr = j * p.G + (hq - hk * p.G);
-  const int rg = rr / kAttnRows, lr = rr - rg * kAttnRows;
-  const size_t part0 = (((size_t)b * p.Hkv + hk) * p.RG + rg) * p.NC;
-  const float2* ml = p.part_ml + part0 * kAttnRows + lr;                    // chunk c at ml[c * 64]
-  const float* po = p.part_o + (part0 * kAttnRows + lr) * D + VEC * lane;   // at po[c * 64 * D]
-  // the chunks' maxima: strided over the threads, then over the block; every
-  // query sees its own key, so some chunk has a finite maximum
-  __shared__ float red_m[NW];
-  __shared__ float red_s[NW][VEC * 32 + 1];   // each warp's sums, then its denominator
+  if (!ok) {
+    // gave up on a stage: report it and let the copies already issued land
+    if (tid == 0) atomicOr(p.err, kErrWaitTimeout);
+    for (int i = done; i < n_mine && i < done + 2; ++i)
+      attn_wait(bars + 8u * (uint32_t)(i & 1), (uint32_t)(i >> 1) & 1u);
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 1);
+    l_run[hh] += __shfl_xor_sync(0xffffffffu, l_run[hh], 2);
+  }
+  // every block is done with its ring (and every copy into it has landed):
+  // the partial results of row r go to block r / 8, into its ring at
+  // [this block][r % 8] (posted stores)
+  cluster_sync_all();
+  {
+    const int rowA = row0 + g, rowB = rowA + 8;   // owners rowA / 8 and rowB / 8
+    const uint32_t slot = (uint32_t)((int)rank * kMergeRows + g);
+    const uint32_t oa = base + SM::OM + slot * SM::O_STRIDE + (uint32_t)tq * 8u;
+    const uint32_t dA = peer_addr(oa, (uint32_t)(rowA / kMergeRows));
+    const uint32_t dB = peer_addr(oa, (uint32_t)(rowB / kMergeRows));
+#pragma unroll
+    for (int nd = 0; nd < D / 8; ++nd) {
+      st_peer_f2(dA + nd * 32, o[nd][0], o[nd][1]);
+      st_peer_f2(dB + nd * 32, o[nd][2], o[nd][3]);
+    }
+    if (tq == 0) {
+      const uint32_t ma = base + SM::ML + slot * 8u;
+      st_peer_f2(peer_addr(ma, (uint32_t)(rowA / kMergeRows)), m_run[0], l_run[0]);
+      st_peer_f2(peer_addr(ma, (uint32_t)(rowB / kMergeRows)), m_run[1], l_run[1]);
+    }
+  }
+  cluster_sync_all();   // every block's partial results have landed
+
+  // merge rows q0 .. q0 + 7 over the cluster's blocks in rank order: sixteen
+  // threads per row; thread q of a row takes the float4s q, q + 16, ... of it
+  // (dimensions 4q .. 4q + 3, ...)
+  constexpr int NV = D / 64;   // float4s per thread
+  constexpr int VEC = 4 * NV;
+  const int r8 = tid / 16, q16 = tid % 16;
+  float2 ml[kCluster];
+  float4 ov[kCluster][NV];
+#pragma unroll
+  for (int c = 0; c < kCluster; ++c) {
+    const uint32_t slot = (uint32_t)(c * kMergeRows + r8);
+    ml[c] = lds64f(base + SM::ML + slot * 8u);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const uint4 w = lds128(base + SM::OM + slot * SM::O_STRIDE + (uint32_t)(q16 + 16 * v) * 16u);
+      ov[c][v] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), __uint_as_float(w.z),
+                             __uint_as_float(w.w));
+    }
+  }
   float mx = -INFINITY;
-  for (int c = tid; c < nc; c += D) mx = fmaxf(mx, ml[(size_t)c * kAttnRows].x);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red_m[w] = mx;
-  __syncthreads();
-  float mmax = red_m[0];
-#pragma unroll
-  for (int i = 1; i < NW; ++i) mmax = fmaxf(mmax, red_m[i]);
+  for (int c = 0; c < kCluster; ++c)
+    if (ml[c].y > 0.f) mx = fmaxf(mx, ml[c].x);
   float acc[VEC], den = 0.f;
 #pragma unroll
   for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-#pragma unroll 4
-  for (int c = w; c < nc; c += NW) {
-    const float2 mc = ml[(size_t)c * kAttnRows];
-    const float* src = po + (size_t)c * kAttnRows * D;
-    float x[VEC];
-    if constexpr (VEC == 4) {
-      const float4 t = *reinterpret_cast<const float4*>(src);
-      x[0] = t.x;
-      x[1] = t.y;
-      x[2] = t.z;
-      x[3] = t.w;
-    } else {
-      const float2 t = *reinterpret_cast<const float2*>(src);
-      x[0] = t.x;
-      x[1] = t.y;
+#pragma unroll
+  for (int c = 0; c < kCluster; ++c) {
+    // a block that saw no visible key of this row adds nothing
+    const float w = ml[c].y > 0.f ? exp2f(ml[c].x - mx) : 0.f;
+    den += w * ml[c].y;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      acc[4 * v] += w * ov[c][v].x;
+      acc[4 * v + 1] += w * ov[c][v].y;
+      acc[4 * v + 2] += w * ov[c][v].z;
+      acc[4 * v + 3] += w * ov[c][v].w;
     }
-    const float wt = exp2f(mc.x - mmax);
-    den += wt * mc.y;
-#pragma unroll
-    for (int v = 0; v < VEC; ++v) acc[v] += wt * x[v];
   }
+
+  const int rr = rr0 + q0 + r8;
+  if (rr < p.R) {
+    const int j = rr / p.G, hq = hk * p.G + (rr - j * p.G);
+    const size_t row = (((size_t)b * p.L + j) * p.Hq + hq) * D;
 #pragma unroll
-  for (int v = 0; v < VEC; ++v) red_s[w][VEC * lane + v] = acc[v];
-  if (lane == 0) red_s[w][VEC * 32] = den;
-  __syncthreads();
-  // thread tid writes dimension tid: the warps' sums in warp order
-  float o = red_s[0][tid], dsum = red_s[0][VEC * 32];
+    for (int v = 0; v < NV; ++v) {
+      const size_t dst = row + 4 * (q16 + 16 * v);
+      if (!in_bounds(dst + 3, p.out_elems, p.err)) continue;
+      uint16_t h[4];
 #pragma unroll
-  for (int i = 1; i < NW; ++i) {
-    o += red_s[i][tid];
-    dsum += red_s[i][VEC * 32];
+      for (int k = 0; k < 4; ++k) h[k] = f2h<kF16>(acc[4 * v + k] / den);
+      if (p.out_vec) {
+        *reinterpret_cast<uint2*>(p.out + dst) =
+            make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16), (uint32_t)h[2] | ((uint32_t)h[3] << 16));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) p.out[dst + k] = h[k];
+      }
+    }
   }
-  dst[tid] = f2h<kF16>(o / dsum);
 }
 
 int attn_check(const void* q, const void* k_new, const void* v_new, const void* k_cache,
@@ -525,11 +776,10 @@ int attn_check(const void* q, const void* k_new, const void* v_new, const void* 
   if (!std::isfinite(scale)) return VQ_EINVAL;
   if (D != 64 && D != 128) return VQ_EUNSUPPORTED;
   if (L > kMaxBlock || S_cap > kMaxCap) return VQ_EUNSUPPORTED;
-  // grid limits: (chunks, Hkv x row groups, B) and (L x Hq, B)
+  // grid limits: (cluster, Hkv x row groups, B); the cache rows are addressed
+  // by 32-bit TMA coordinates
   const long long row_groups = ((long long)L * (Hq / Hkv) + kAttnRows - 1) / kAttnRows;
-  // (the cache rows are addressed by 32-bit TMA coordinates)
-  if ((long long)Hkv * row_groups > 65535 || B > 65535 || (long long)L * Hq > 0x7fffffffll ||
-      (long long)B * Hkv * S_cap > 0x7fffffffll)
+  if ((long long)Hkv * row_groups > 65535 || B > 65535 || (long long)B * Hkv * S_cap > 0x7fffffffll)
     return VQ_EUNSUPPORTED;
   const uintptr_t a16 = (uintptr_t)q | (uintptr_t)k_new | (uintptr_t)v_new |
                         (uintptr_t)k_cache | (uintptr_t)v_cache;
@@ -540,66 +790,26 @@ int attn_check(const void* q, const void* k_new, const void* v_new, const void* 
 }
 
 struct AttnShape {
-  int G, R, RG, NC;
+  int G, R, RG;
 };
 
-AttnShape attn_shape(int L, int Hq, int Hkv, int S_cap) {
+AttnShape attn_shape(int L, int Hq, int Hkv) {
   AttnShape s;
   s.G = Hq / Hkv;
   s.R = L * s.G;
   s.RG = (s.R + kAttnRows - 1) / kAttnRows;
-  s.NC = (S_cap + kChunk - 1) / kChunk;
   return s;
-}
-
-size_t attn_part_count(int B, int Hkv, const AttnShape& s) {
-  return (size_t)B * Hkv * s.RG * s.NC * kAttnRows;
-}
-
-// Byte offset of the rotated queries in the workspace (rows: partial-result rows).
-size_t attn_qrot_offset(size_t rows, int D) {
-  return (rows * (size_t)D * sizeof(float) + rows * sizeof(float2) + 15) / 16 * 16;
 }
 
 template <bool kF16, int D>
 int attn_launch(const AttnParams& p, int B, cudaStream_t stream, const CUtensorMap& tm_k,
                 const CUtensorMap& tm_v) {
-  // three swizzled tiles (1 KiB-aligned) and two mbarriers
-  const size_t smem = 1024 + (size_t)3 * kAttnRows * D * 2 + 16;
-  auto* partial = verify_attn_partial_kernel<kF16, D>;
-  if (ensure_smem<verify_attn_partial_kernel<kF16, D>>(smem) != VQ_OK) return VQ_ECUDA;
-  // the rotation runs after everything before it in the stream; the partial
-  // kernel may be scheduled while it runs and waits for it on the GPU
-  verify_attn_rope_kernel<kF16, D><<<dim3(p.L, B), kRopeThreads, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return VQ_ECUDA;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.NC, p.Hkv * p.RG, B);
-    cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, partial, tm_k, tm_v, p) != cudaSuccess) return VQ_ECUDA;
-  }
-  // the merge may be scheduled while the partial kernel runs; it waits for it
-  // (griddepcontrol.wait) before reading anything
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.L * p.Hq, B);
-  cfg.blockDim = dim3(D);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, verify_attn_combine_kernel<kF16, D>, p) != cudaSuccess)
-    return VQ_ECUDA;
-  return VQ_OK;
+  const size_t smem = 1024 + AttnSmem<D>::BYTES;   // + the 1 KiB alignment of the base
+  if (ensure_smem<verify_attn_kernel<kF16, D>>(smem) != VQ_OK) return VQ_ECUDA;
+  // clusters of kCluster blocks along x (the kernel's compile-time cluster shape)
+  verify_attn_kernel<kF16, D>
+      <<<dim3(kCluster, p.Hkv * p.RG, B), kAttnThreads, smem, stream>>>(tm_k, tm_v, p);
+  return cudaGetLastError() == cudaSuccess ? VQ_OK : VQ_ECUDA;
 }
 
 }  // namespace
@@ -607,13 +817,8 @@ int attn_launch(const AttnParams& p, int B, cudaStream_t stream, const CUtensorM
 
 using namespace vq;
 
-extern "C" size_t verify_attention_workspace_bytes(int B, int L, int Hq, int Hkv, int D,
-                                                   int S_cap) {
-  if (B < 1 || L < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || S_cap < 1) return 0;
-  const AttnShape s = attn_shape(L, Hq, Hkv, S_cap);
-  const size_t rows = attn_part_count(B, Hkv, s);
-  // [partial outputs][partial (max, sum)][rotated queries], each 16-byte aligned
-  return attn_qrot_offset(rows, D) + (size_t)B * Hkv * s.RG * kAttnRows * D * sizeof(uint16_t);
+extern "C" size_t verify_attention_workspace_bytes(int, int, int, int, int, int) {
+  return 0;   // the kernel keeps its partial results in the cluster's shared memory
 }
 
 extern "C" int verify_attention(const void* q, const void* k_new, const void* v_new,
@@ -625,13 +830,13 @@ extern "C" int verify_attention(const void* q, const void* k_new, const void* v_
   int rc = attn_check(q, k_new, v_new, k_cache, v_cache, prefix_len, src_off, out, B, L, Hq, Hkv,
                       D, S_cap, rotary_dim, theta, scale, dtype, status);
   if (rc) return rc;
-  const size_t need = verify_attention_workspace_bytes(B, L, Hq, Hkv, D, S_cap);
-  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 15u)) return VQ_EWORKSPACE;
+  (void)workspace;   // none needed
+  (void)workspace_bytes;
   int32_t* err = nullptr;   // the device's status word (a usable current device)
   rc = device_error_word(&err);
   if (rc) return rc;
 
-  const AttnShape s = attn_shape(L, Hq, Hkv, S_cap);
+  const AttnShape s = attn_shape(L, Hq, Hkv);
   AttnParams p{};
   p.q = static_cast<const uint16_t*>(q);
   p.k_new = static_cast<const uint16_t*>(k_new);
@@ -643,22 +848,15 @@ extern "C" int verify_attention(const void* q, const void* k_new, const void* v_
   p.out = static_cast<uint16_t*>(out);
   p.status = status;
   p.err = err;
-  const size_t rows = attn_part_count(B, Hkv, s);
-  p.part_o = static_cast<float*>(workspace);
-  p.part_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
-                                        rows * (size_t)D * sizeof(float));
-  p.q_rot = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + attn_qrot_offset(rows, D));
   p.cache_elems = (size_t)B * Hkv * S_cap * D;
   p.out_elems = (size_t)B * L * Hq * D;
-  p.part_rows = rows;
-  p.qrot_bytes = (size_t)B * Hkv * s.RG * kAttnRows * D * sizeof(uint16_t);
+  p.out_vec = ((uintptr_t)out & 15u) == 0;
   p.L = L;
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.G = s.G;
   p.R = s.R;
   p.RG = s.RG;
-  p.NC = s.NC;
   p.S_cap = S_cap;
   p.rot_half = rotary_dim / 2;
   p.scale_log2 = (float)(scale * 1.4426950408889634);   // log2(e)

@@ -117,25 +117,17 @@ def test_host_validation_rejects_before_any_launch(vqlib):
 
 def test_verify_attention_workspace_and_host_validation(vqlib):
     P = ctypes.c_void_p
-    # rows of partial results: B * Hkv * ceil(L*G/64) * ceil(S_cap/64) * 64, each
-    # D floats of output plus (max, sum); then the rotated queries as one tile
-    # of 64 rows x D 16-bit values per (row, KV head, group of 64 query rows)
-    rows = 4 * 8 * 1 * 32 * 64
-    assert vqlib.verify_attention_workspace_bytes(4, 16, 32, 8, 128, 2048) == \
-        rows * (128 * 4 + 8) + 4 * 8 * 1 * 64 * 128 * 2
-    rows = 2 * 2 * 2 * 2 * 64                      # L*G = 80 rows -> two groups of 64
-    assert vqlib.verify_attention_workspace_bytes(2, 10, 16, 2, 64, 100) == \
-        rows * (64 * 4 + 8) + 2 * 2 * 2 * 64 * 64 * 2
-    assert vqlib.verify_attention_workspace_bytes(2, 10, 15, 2, 64, 100) == 0
+    # the partial results stay in the clusters' shared memory: no workspace
+    assert vqlib.verify_attention_workspace_bytes(4, 16, 32, 8, 128, 2048) == 0
+    assert vqlib.verify_attention_workspace_bytes(2, 10, 16, 2, 64, 100) == 0
 
     fake = P(0x1000)
-    ws_need = vqlib.verify_attention_workspace_bytes(4, 16, 32, 8, 128, 2048)
 
     def call(q=fake, out=fake, B=4, L=16, Hq=32, Hkv=8, D=128, S_cap=2048, rd=128, theta=1e6,
-             scale=0.088, dtype=1, ws=fake, ws_bytes=ws_need):
+             scale=0.088, dtype=1):
         # every call below fails validation before any CUDA work
         return vqlib.verify_attention(q, fake, fake, fake, fake, fake, fake, out, B, L, Hq, Hkv, D,
-                                      S_cap, rd, theta, scale, dtype, None, ws, ws_bytes, None)
+                                      S_cap, rd, theta, scale, dtype, None, None, 0, None)
 
     assert call(B=0) == -1
     assert call(Hq=30) == -1                       # not a multiple of Hkv
@@ -149,9 +141,6 @@ def test_verify_attention_workspace_and_host_validation(vqlib):
     assert call(L=65, S_cap=4096) == -4
     assert call(q=P(0x1008)) == -2                 # 16-byte alignment
     assert call(out=P(0x1001)) == -2
-    assert call(ws=None) == -5
-    assert call(ws_bytes=ws_need - 1) == -5
-    assert call(ws=P(0x1008)) == -5
 
 
 def test_wait_selftest_host_validation(vqlib):
