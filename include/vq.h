@@ -118,6 +118,26 @@ int vq_linear(const void* x, int M, int K, int N, const uint32_t* qw, const uint
               size_t workspace_bytes, void* stream);
 
 /*
+ * vq_linear for activations and outputs in host memory: enqueues on `stream`
+ * the copy of x_host into x_dev, vq_linear(x_dev -> y_dev) and the copy of
+ * y_dev into y_host, and returns (nothing is waited for; the caller
+ * synchronizes the stream before reading y_host). For the step a serving
+ * loop makes when the activations arrive from and the logits go back to the
+ * host.
+ *
+ * x_host   [M][K] in act_dtype, host memory (page-locked for the copies to
+ *          be asynchronous). y_host [M][N] in act_dtype, host memory.
+ * x_dev, y_dev  device buffers of the same shapes, with vq_linear's
+ *          alignment (16 bytes for x_dev, 4 for y_dev); owned by the caller.
+ * Other arguments as vq_linear. Shape errors are returned before anything
+ * is enqueued; VQ_ECUDA if a copy cannot be enqueued.
+ */
+int vq_linear_host(const void* x_host, int M, int K, int N, const uint32_t* qw,
+                   const uint16_t* scales, const uint16_t* biases, void* y_host, int act_dtype,
+                   void* x_dev, void* y_dev, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
+/*
  * Vocabulary projection with a fused greedy arg max.
  *
  * Source: dflash-mlx #7, PR description (the W4A32 vocabulary projection of

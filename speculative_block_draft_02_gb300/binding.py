@@ -29,6 +29,7 @@ _P, _I, _S, _D = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_double
 SIGNATURES = {
     "vq_linear_workspace_bytes": (_S, [_I, _I, _I, _I]),
     "vq_linear": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _P, _S, _P]),
+    "vq_linear_host": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _I, _P, _P, _P, _S, _P]),
     "vq_vocab_argmax_workspace_bytes": (_S, [_I]),
     "vq_vocab_argmax": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P, _S, _P]),
     "vq_vocab_argmax_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P, _P]),
@@ -132,6 +133,26 @@ def vq_linear(x, qw, scales, biases, y=None, workspace=None, stream=None):
                          _ACT[x.dtype], _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "vq_linear")
     return y
+
+
+def vq_linear_host(x_host, qw, scales, biases, y_host, x_dev, y_dev, workspace=None, stream=None):
+    """vq_linear with x and y in page-locked host memory: enqueues the copy of
+    x_host into x_dev, the projection into y_dev and the copy into y_host on
+    the stream (synchronize it before reading y_host)."""
+    M, K = x_host.shape
+    N = qw.shape[0]
+    for t in (x_host, y_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise VQError("expected a contiguous host tensor")
+    if x_dev.shape != x_host.shape or y_dev.shape != y_host.shape or x_dev.dtype != x_host.dtype \
+            or y_dev.dtype != y_host.dtype:
+        raise VQError("device buffers must match the host tensors' shapes and dtypes")
+    ws_bytes = 0 if workspace is None else workspace.nbytes
+    rc = lib().vq_linear_host(x_host.data_ptr(), M, K, N, _ptr(qw), _ptr(scales), _ptr(biases),
+                              y_host.data_ptr(), _ACT[x_host.dtype], _ptr(x_dev), _ptr(y_dev),
+                              _ptr(workspace), ws_bytes, _stream(stream))
+    _check(rc, "vq_linear_host")
+    return y_host
 
 
 def vq_vocab_argmax(x, qw, scales, biases, workspace, argmax=None, maxval=None, stream=None):

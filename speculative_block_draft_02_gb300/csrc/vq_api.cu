@@ -94,7 +94,8 @@ int encode(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, int rank,
   }
   for (int i = 0; i + 1 < rank; ++i) k.strides[i] = strides[i];
   for (int i = 0; i < t_tm_used; ++i) {
-    if (memcmp(&t_tm[i].key, &k, sizeof k) == 0) {
+    // the address first: a lookup scans up to kTmCache entries on every call
+    if (t_tm[i].key.ptr == ptr && memcmp(&t_tm[i].key, &k, sizeof k) == 0) {
       *m = t_tm[i].map;
       return VQ_OK;
     }
@@ -431,8 +432,12 @@ int run_gemm(const void* x, int M, int K, int N, const uint32_t* qw, const uint1
   }
   const int eb = f32 ? 4 : 2;
   // box rows = 8*MT >= M: the rows past M are out of range and arrive zeroed;
-  // the x-table variant takes every group of K in one box
-  if (encode_x3d(&L.tm_x, xdt, x, M, K, eb, pl.MP, pl.xm == 1 ? K / 64 : kBK / (128 / eb)) == VQ_OK) {
+  // the x-table variant takes every group of K in one box. The prepared-slice
+  // plan reads x only in the slice kernel (plain loads): no map.
+  if (pl.xm == 2) {
+    memset(&L.tm_x, 0, sizeof L.tm_x);
+    p.x3d = 0;
+  } else if (encode_x3d(&L.tm_x, xdt, x, M, K, eb, pl.MP, pl.xm == 1 ? K / 64 : kBK / (128 / eb)) == VQ_OK) {
     p.x3d = 1;
   } else {
     if ((rc = encode_2d(&L.tm_x, xdt, x, (uint64_t)K, (uint64_t)M, (uint64_t)K * eb, 128 / eb,
@@ -484,6 +489,67 @@ extern "C" int vq_linear(const void* x, int M, int K, int N, const uint32_t* qw,
                          void* workspace, size_t workspace_bytes, void* stream) {
   return run_gemm(x, M, K, N, qw, scales, biases, act_dtype, false, y, nullptr, nullptr,
                   workspace, workspace_bytes, stream);
+}
+
+namespace {
+// The device address of page-locked host memory that the current device can
+// address (false for anything else; the error a failed query leaves is cleared).
+bool device_view(const void* h, void** d) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return false;
+  *d = a.devicePointer;
+  return true;
+}
+}  // namespace
+
+extern "C" int vq_linear_host(const void* x_host, int M, int K, int N, const uint32_t* qw,
+                              const uint16_t* scales, const uint16_t* biases, void* y_host,
+                              int act_dtype, void* x_dev, void* y_dev, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (!x_host || !y_host || !x_dev || !y_dev) return VQ_EINVAL;
+  if (M < 1 || K < 1 || N < 1) return VQ_EINVAL;
+  if (act_dtype != VQ_BF16 && act_dtype != VQ_F16 && act_dtype != VQ_F32) return VQ_EINVAL;
+  const size_t eb = act_dtype == VQ_F32 ? 4 : 2;
+  const size_t x_bytes = (size_t)M * K * eb, y_bytes = (size_t)M * N * eb;
+  // the shape, the device buffers and the workspace are checked before
+  // anything is enqueued (the weights' arguments by vq_linear itself)
+  int sms = 0;
+  int rc = device_state(&sms, nullptr);
+  if (rc) return rc;
+  Plan pl;
+  if ((rc = make_plan(M, K, N, act_dtype, false, sms, &pl))) return rc;
+  if (((uintptr_t)x_dev & 15u) || ((uintptr_t)y_dev & 3u)) return VQ_EALIGN;
+  const size_t need = pl.ws_bytes;
+  if (need && (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 15u)))
+    return VQ_EWORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Where the device can address the page-locked host buffers (unified
+  // addressing; on a coherent CPU-GPU link as on GB300 at full link speed),
+  // the prepared-slice plan's slice kernel reads x from them directly and,
+  // without a K split, the projection writes y into them directly; otherwise
+  // (and for every other plan) the buffers are copied through x_dev and y_dev.
+  const void* xs = x_dev;
+  void* yd = y_dev;
+  void* xv = nullptr;
+  void* yv = nullptr;
+  const bool zx = pl.xm == 2 && device_view(x_host, &xv) && !((uintptr_t)xv & 15u);
+  const bool zy = pl.xm == 2 && pl.S == 1 && device_view(y_host, &yv) && !((uintptr_t)yv & 3u);
+  if (zx) {
+    xs = xv;
+  } else if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+    return VQ_ECUDA;
+  }
+  if (zy) yd = yv;
+  rc = run_gemm(xs, M, K, N, qw, scales, biases, act_dtype, false, yd, nullptr, nullptr, workspace,
+                workspace_bytes, stream);
+  if (rc || zy) return rc;
+  return cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, st) == cudaSuccess
+             ? VQ_OK
+             : VQ_ECUDA;
 }
 
 extern "C" size_t vq_vocab_argmax_workspace_bytes(int M) {

@@ -1162,7 +1162,7 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
           prefetch_tensormap(&tm_s);
           prefetch_tensormap(&tm_b);
         }
-        prefetch_tensormap(&tm_x);
+        if (!XS) prefetch_tensormap(&tm_x);   // prepared slices: x is not read by TMA
       }
       // Weights are constants of the model: the first stages' weights are
       // requested before waiting for the kernel before this one in the stream

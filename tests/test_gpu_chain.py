@@ -89,3 +89,30 @@ def test_argmax_after_projection_reads_its_output(M, K1, N1, N2):
     assert torch.equal(idx, ridx)
     assert torch.equal(mx, rmx)
     assert not wsa.any()
+
+
+
+@pytest.mark.parametrize("M,K,N,dtype", [(8, 5120, 17408, "bf16"), (3, 512, 1000, "f16"),
+                                         (7, 1024, 500, "f32"), (64, 1024, 9800, "bf16"),
+                                         (8, 5120, 1024, "bf16")])
+def test_linear_host_buffers_match_device_call(M, K, N, dtype):
+    """vq_linear_host (x in and y out through page-locked host memory, enqueued
+    with the projection) gives what vq_linear gives on the same inputs, bit for
+    bit, twice in a row on the same buffers and workspace (narrow N splits K,
+    so the workspace must come back zeroed)."""
+    from parity import to_dev_act
+
+    qw, s, b = _dev_weights(M + K + N, N, K)
+    x = to_dev_act(synth.activations(M + K + N, M, K, dtype), dtype)
+    nb = vq.vq_linear_workspace_bytes(M, K, N, x.dtype)
+    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
+    y_ref = vq.vq_linear(x, qw, s, b, workspace=ws).cpu()
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty((M, N), dtype=x.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    y_dev = torch.empty((M, N), dtype=x.dtype, device="cuda")
+    for _ in range(2):
+        y_host.fill_(float("nan"))
+        vq.vq_linear_host(x_host, qw, s, b, y_host, x_dev, y_dev, workspace=ws)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(y_host.view(torch.uint8), y_ref.view(torch.uint8))
