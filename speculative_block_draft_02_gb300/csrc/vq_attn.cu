@@ -684,13 +684,35 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   {
     const int rowA = row0 + g, rowB = rowA + 8;   // owners rowA / 8 and rowB / 8
     const uint32_t slot = (uint32_t)((int)rank * kMergeRows + g);
-    const uint32_t oa = base + SM::OM + slot * SM::O_STRIDE + (uint32_t)tq * 8u;
+    // the two threads tq, tq ^ 1 trade halves so that each holds four
+    // consecutive dimensions: the even one those of 8-column tile 2k, the odd
+    // one those of tile 2k + 1 (one shuffle per value, half the stores)
+    const bool odd = (tq & 1) != 0;
+    const uint32_t oa = base + SM::OM + slot * SM::O_STRIDE +
+                        (uint32_t)((odd ? 8 + 2 * (tq - 1) : 2 * tq) * 4);
     const uint32_t dA = peer_addr(oa, (uint32_t)(rowA / kMergeRows));
     const uint32_t dB = peer_addr(oa, (uint32_t)(rowB / kMergeRows));
 #pragma unroll
-    for (int nd = 0; nd < D / 8; ++nd) {
-      st_peer_f2(dA + nd * 32, o[nd][0], o[nd][1]);
-      st_peer_f2(dB + nd * 32, o[nd][2], o[nd][3]);
+    for (int k = 0; k < D / 16; ++k) {
+      float t[4], keep[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // the half the partner takes goes over, the other half stays
+        t[e] = __shfl_xor_sync(0xffffffffu, odd ? o[2 * k][e] : o[2 * k + 1][e], 1);
+        keep[e] = odd ? o[2 * k + 1][e] : o[2 * k][e];
+      }
+      float4 va, vb;
+      if (odd) {
+        va = make_float4(t[0], t[1], keep[0], keep[1]);
+        vb = make_float4(t[2], t[3], keep[2], keep[3]);
+      } else {
+        va = make_float4(keep[0], keep[1], t[0], t[1]);
+        vb = make_float4(keep[2], keep[3], t[2], t[3]);
+      }
+      st_peer_v4(dA + k * 64, make_uint4(__float_as_uint(va.x), __float_as_uint(va.y),
+                                         __float_as_uint(va.z), __float_as_uint(va.w)));
+      st_peer_v4(dB + k * 64, make_uint4(__float_as_uint(vb.x), __float_as_uint(vb.y),
+                                         __float_as_uint(vb.z), __float_as_uint(vb.w)));
     }
     if (tq == 0) {
       const uint32_t ma = base + SM::ML + slot * 8u;
