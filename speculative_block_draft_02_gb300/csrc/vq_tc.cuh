@@ -616,46 +616,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w};
         const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-        // two groups per step (buffers b, b+1): both accumulators are read
-        // with one wait, so their load latencies overlap
+        // one group per step (buffer j & 3): its accumulator is read, the
+        // buffer released, then folded (one group's HC registers at a time
+        // keeps the fold warps within their register budget)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int G = 8 * q + 2 * jj;
-          const int b = (2 * jj) & 3;
+        for (int j = 0; j < 8; ++j) {
+          const int G = 8 * q + j;
+          const int b = j & 3;
           const uint32_t ph = (uint32_t)(G / kTcBufs) & 1u;
           if (!aborted && !wait_or_abort(mdone_bar(b), ph, abort_flag, p.err)) aborted = true;
-          if (!aborted && !wait_or_abort(mdone_bar(b + 1), ph, abort_flag, p.err)) aborted = true;
-          uint32_t acc0[HC], acc1[HC];
+          uint32_t acc[HC];
           if (!aborted) {
             tc_fence_after();
-            tc_ld<HC>(tmem + tl + kTcDCol + (uint32_t)(MP * b + HC * ch), acc0);
-            tc_ld<HC>(tmem + tl + kTcDCol + (uint32_t)(MP * (b + 1) + HC * ch), acc1);
+            tc_ld<HC>(tmem + tl + kTcDCol + (uint32_t)(MP * b + HC * ch), acc);
             tc_wait_ld();
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(dempty_bar(b));
-            mbar_arrive(dempty_bar(b + 1));
-          }
+          if (lane == 0) mbar_arrive(dempty_bar(b));
           if (!aborted) {
+            const uint32_t s2 = sw[j >> 1], b2 = bw[j >> 1];
+            const bool h = (j & 1) != 0;
+            const float s = __uint_as_float(h ? (s2 & 0xFFFF0000u) : (s2 << 16));
+            const float bb = __uint_as_float(h ? (b2 & 0xFFFF0000u) : (b2 << 16));
+            const float c = fmaf(-kC0, s, bb);   // exact: bias - c0*scale
+            const float4* xs4 = reinterpret_cast<const float4*>(xs_base + j * MP + HC * ch);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int j = 2 * jj + h;
-              const uint32_t s2 = sw[jj], b2 = bw[jj];
-              const float s = __uint_as_float(h ? (s2 & 0xFFFF0000u) : (s2 << 16));
-              const float bb = __uint_as_float(h ? (b2 & 0xFFFF0000u) : (b2 << 16));
-              const float c = fmaf(-kC0, s, bb);   // exact: bias - c0*scale
-              const float4* xs4 = reinterpret_cast<const float4*>(xs_base + j * MP + HC * ch);
-              const uint32_t* acc = h ? acc1 : acc0;
-#pragma unroll
-              for (int i4 = 0; i4 < HC / 4; ++i4) {
-                const float4 xs = xs4[i4];
-                tot[4 * i4 + 0] = fmaf(s, __uint_as_float(acc[4 * i4 + 0]), fmaf(c, xs.x, tot[4 * i4 + 0]));
-                tot[4 * i4 + 1] = fmaf(s, __uint_as_float(acc[4 * i4 + 1]), fmaf(c, xs.y, tot[4 * i4 + 1]));
-                tot[4 * i4 + 2] = fmaf(s, __uint_as_float(acc[4 * i4 + 2]), fmaf(c, xs.z, tot[4 * i4 + 2]));
-                tot[4 * i4 + 3] = fmaf(s, __uint_as_float(acc[4 * i4 + 3]), fmaf(c, xs.w, tot[4 * i4 + 3]));
-              }
+            for (int i4 = 0; i4 < HC / 4; ++i4) {
+              const float4 xs = xs4[i4];
+              tot[4 * i4 + 0] = fmaf(s, __uint_as_float(acc[4 * i4 + 0]), fmaf(c, xs.x, tot[4 * i4 + 0]));
+              tot[4 * i4 + 1] = fmaf(s, __uint_as_float(acc[4 * i4 + 1]), fmaf(c, xs.y, tot[4 * i4 + 1]));
+              tot[4 * i4 + 2] = fmaf(s, __uint_as_float(acc[4 * i4 + 2]), fmaf(c, xs.z, tot[4 * i4 + 2]));
+              tot[4 * i4 + 3] = fmaf(s, __uint_as_float(acc[4 * i4 + 3]), fmaf(c, xs.w, tot[4 * i4 + 3]));
             }
           }
         }
