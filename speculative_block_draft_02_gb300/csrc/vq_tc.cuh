@@ -156,6 +156,12 @@ __device__ __forceinline__ void tc_ld(uint32_t taddr, uint32_t (&r)[N]) {
         : "memory");
   }
 }
+__device__ __forceinline__ uint32_t lds32_at(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ uint4 lds128_at(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -618,8 +624,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
         // one group per step (buffer j & 3): its accumulator is read, the
         // buffer released, then folded (one group's HC registers at a time
-        // keeps the fold warps within their register budget)
-#pragma unroll
+        // keeps the fold warps within their register budget). The arg max
+        // keeps this loop rolled (its larger epilogue already fills the
+        // instruction cache: 3 % faster measured), the projection unrolls it.
+#pragma unroll(ARGMAX ? 1 : 8)
         for (int j = 0; j < 8; ++j) {
           const int G = 8 * q + j;
           const int b = j & 3;
@@ -635,7 +643,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(dempty_bar(b));
           if (!aborted) {
-            const uint32_t s2 = sw[j >> 1], b2 = bw[j >> 1];
+            uint32_t s2, b2;
+            if constexpr (ARGMAX) {   // rolled loop: from shared memory, not indexed registers
+              s2 = lds32_at(sb + kTcOffS + (uint32_t)nl * 16u + (uint32_t)(j >> 1) * 4u);
+              b2 = lds32_at(sb + kTcOffB + (uint32_t)nl * 16u + (uint32_t)(j >> 1) * 4u);
+            } else {
+              s2 = sw[j >> 1];
+              b2 = bw[j >> 1];
+            }
             const bool h = (j & 1) != 0;
             const float s = __uint_as_float(h ? (s2 & 0xFFFF0000u) : (s2 << 16));
             const float bb = __uint_as_float(h ? (b2 & 0xFFFF0000u) : (b2 << 16));
