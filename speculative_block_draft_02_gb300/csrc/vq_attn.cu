@@ -289,9 +289,10 @@ __device__ __forceinline__ bool attn_wait(uint32_t bar, uint32_t parity) {
 // (keys, values), the (cos, sin) table of the prefetched block keys, those
 // block rows of this block's boundary chunk (keys, then values, as given),
 // the rotation frequencies, the (cos, sin) table of this block's query rows'
-// positions and two mbarriers. After the last chunk the
-// ring holds the block's partial results: the unnormalised outputs
-// [64][D + 4] fp32 (rows padded against bank conflicts), then (max, sum) [64].
+// positions and two mbarriers. Once every block of the cluster is done with its
+// chunks, the ring receives the partial results the cluster's blocks send for
+// this block's eight query rows, at [sender][row]: the unnormalised outputs
+// [8][8][D + 4] fp32 (rows padded against bank conflicts), then (max, sum) [8][8].
 template <int D>
 struct AttnSmem {
   static constexpr uint32_t TILE = kAttnRows * D * 2;

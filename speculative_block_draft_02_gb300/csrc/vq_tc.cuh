@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // made exact (one fp16 subtraction per pair) and c0 = 0.
   constexpr bool kExact = ARGMAX && kF16;
   constexpr float kC0 = kExact ? 0.f : kF16 ? 1024.f : 128.f;
-  constexpr int HC = MP / 4;   // accumulator columns per fold warp
+  constexpr int HC = MP / (kTcFoldWarps / 4);   // accumulator columns per fold warp
   constexpr uint32_t kIdesc = tc_idesc(!kF16, MP);
   static_assert(MP == 32 || MP == 64, "MP");
 
@@ -577,10 +577,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // ------------------------------------------------------------------ fold
     const int f = warp - kTcUnpackWarps;
-    const int qd = f & 3, ch = f >> 2;   // lane quarter, column quarter
+    const int qd = f & 3, ch = f >> 2;   // lane quarter, column chunk
     const int nl = 32 * qd + lane;
     const uint32_t tl = (uint32_t)(32 * qd) << 16;
-    const int ft = f * 32 + lane;   // 0..511 over the fold warps
+    const int ft = f * 32 + lane;   // 0 .. 32 * kTcFoldWarps - 1 over the fold warps
     bool aborted = false;
     // x and every output may belong to the kernel before this one
     grid_wait_prerequisites();
@@ -608,10 +608,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float* xs_base = xs_tab + kt * 8 * MP;
         if (p.xs_stage || (ARGMAX && u == (int)blockIdx.x)) {
           float* dst = p.xs_stage ? xs_tab + (q & 1) * 8 * MP : xs_tab + kt * 8 * MP;
-          if (!aborted && ft < 8 * MP) {
-            const int j = ft / MP, m = ft - j * MP;
-            dst[j * MP + m] = tc_group_sum_smem<ACT, MP>(sb + kTcOffX, j, m);
-          }
+          if (!aborted)
+            for (int e = ft; e < 8 * MP; e += kTcFoldWarps * 32) {
+              const int j = e / MP, m = e - j * MP;
+              dst[j * MP + m] = tc_group_sum_smem<ACT, MP>(sb + kTcOffX, j, m);
+            }
           named_bar_sync(1, kTcFoldWarps * 32);
           xs_base = dst;
         }
