@@ -149,3 +149,18 @@ def test_wait_selftest_host_validation(vqlib):
     assert vqlib.vq_wait_selftest(P(0x1000), None, None) == -1
     assert vqlib.vq_wait_selftest(P(0x1002), P(0x1000), None) == -2
     assert vqlib.vq_wait_selftest(P(0x1000), P(0x1004), None) == -2
+
+
+def test_linear_host_validation(vqlib):
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+
+    def call(xh=fake, yh=fake, xd=fake, yd=fake, M=8, K=512, N=128, act=0):
+        # every call below fails validation before any CUDA work
+        return vqlib.vq_linear_host(xh, M, K, N, fake, fake, fake, yh, act, xd, yd, None, 0, None)
+
+    assert call(xh=None) == -1
+    assert call(yh=None) == -1
+    assert call(xd=None) == -1 and call(yd=None) == -1
+    assert call(M=0) == -1 and call(K=0) == -1 and call(N=0) == -1
+    assert call(act=7) == -1

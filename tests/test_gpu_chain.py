@@ -116,3 +116,27 @@ def test_linear_host_buffers_match_device_call(M, K, N, dtype):
         vq.vq_linear_host(x_host, qw, s, b, y_host, x_dev, y_dev, workspace=ws)
         torch.cuda.current_stream().synchronize()
         assert torch.equal(y_host.view(torch.uint8), y_ref.view(torch.uint8))
+
+
+def test_linear_host_pageable_and_mixed_buffers():
+    """Host buffers the device cannot address directly (ordinary pageable memory)
+    go through the copies: same bits as vq_linear, with pageable x and pinned y
+    and the other way round."""
+    from parity import to_dev_act
+
+    M, K, N = 8, 5120, 17408
+    qw, s, b = _dev_weights(91, N, K)
+    x = to_dev_act(synth.activations(91, M, K, "bf16"), "bf16")
+    nb = vq.vq_linear_workspace_bytes(M, K, N, x.dtype)
+    ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
+    y_ref = vq.vq_linear(x, qw, s, b, workspace=ws).cpu()
+    x_dev = torch.empty_like(x)
+    y_dev = torch.empty((M, N), dtype=x.dtype, device="cuda")
+    for x_pin, y_pin in ((False, False), (False, True), (True, False)):
+        x_host = x.cpu().pin_memory() if x_pin else x.cpu().clone()
+        y_host = torch.full((M, N), float("nan"), dtype=x.dtype)
+        if y_pin:
+            y_host = y_host.pin_memory()
+        vq.vq_linear_host(x_host, qw, s, b, y_host, x_dev, y_dev, workspace=ws)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(y_host.view(torch.uint8), y_ref.view(torch.uint8)), (x_pin, y_pin)
