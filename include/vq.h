@@ -129,8 +129,14 @@ int vq_linear(const void* x, int M, int K, int N, const uint32_t* qw, const uint
  *          be asynchronous). y_host [M][N] in act_dtype, host memory.
  * x_dev, y_dev  device buffers of the same shapes, with vq_linear's
  *          alignment (16 bytes for x_dev, 4 for y_dev); owned by the caller.
- * Other arguments as vq_linear. Shape errors are returned before anything
- * is enqueued; VQ_ECUDA if a copy cannot be enqueued.
+ * Other arguments as vq_linear. Errors in the shape, the device buffers and
+ * the workspace are returned before anything is enqueued; an error in the
+ * weights' arguments (as vq_linear returns it) may come after the copy of x
+ * has been enqueued; VQ_ECUDA if a copy cannot be enqueued. Where the device
+ * can address page-locked host buffers directly (cudaPointerGetAttributes;
+ * with unified addressing, as on GB300), the plans that read x only in their
+ * slice kernel read it from x_host and, without a K split, write y straight
+ * into y_host; x_dev and y_dev are then not touched.
  */
 int vq_linear_host(const void* x_host, int M, int K, int N, const uint32_t* qw,
                    const uint16_t* scales, const uint16_t* biases, void* y_host, int act_dtype,
