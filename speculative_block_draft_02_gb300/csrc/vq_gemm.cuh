@@ -358,6 +358,17 @@ __device__ __forceinline__ void store_out(void* y, size_t i, float v) {
   }
 }
 
+// Two adjacent 16-bit outputs (index i even) as one 4-byte store.
+template <int ACT>
+__device__ __forceinline__ void store_out2(void* y, size_t i, float a, float b) {
+  if constexpr (ACT == VQ_BF16) {
+    *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(y) + i) =
+        __floats2bfloat162_rn(a, b);
+  } else if constexpr (ACT == VQ_F16) {
+    *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(y) + i) = __floats2half2_rn(a, b);
+  }
+}
+
 // Order-preserving 32-bit image of a (non-NaN) float; -0 is folded into +0
 // by the caller so that equal values compare equal.
 __device__ __forceinline__ uint32_t float_order(float v) {
@@ -1401,16 +1412,29 @@ __global__ void __launch_bounds__(Cfg<MT, WIDE>::THREADS, 1)
       // (the WIDE layout is only launched without a K split)
       if (WIDE != 0 || p.S == 1) {
         if (!aborted) {
+          // a lane holds columns n, n + 1 of rows m: with 16-bit y and an even
+          // N they go out as one 4-byte store, so that the eight lanes of a
+          // row fill whole 32-byte sectors (this matters when y is host memory)
+          const bool pair = ACT != VQ_F32 && (p.N & 1) == 0;
 #pragma unroll
           for (int r = 0; r < RT; ++r)
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g + (e >> 1);
-                const int m = 8 * mt + 2 * t + (e & 1);
-                if (n < p.N && m < p.M && in_bounds((size_t)m * p.N + n, p.y_elems, p.err))
-                  store_out<ACT>(p.y, (size_t)m * p.N + n, tot[r][mt][e]);
+              for (int h = 0; h < 2; ++h) {
+                const int n = rb * kBN + 16 * (RT * rw + r) + 2 * g;
+                const int m = 8 * mt + 2 * t + h;
+                if (m >= p.M) continue;
+                const size_t i = (size_t)m * p.N + n;
+                if (pair && n + 1 < p.N) {
+                  if (in_bounds(i + 1, p.y_elems, p.err))
+                    store_out2<ACT>(p.y, i, tot[r][mt][h], tot[r][mt][h + 2]);
+                } else {
+                  if (n < p.N && in_bounds(i, p.y_elems, p.err))
+                    store_out<ACT>(p.y, i, tot[r][mt][h]);
+                  if (n + 1 < p.N && in_bounds(i + 1, p.y_elems, p.err))
+                    store_out<ACT>(p.y, i + 1, tot[r][mt][h + 2]);
+                }
               }
         }
       } else {
