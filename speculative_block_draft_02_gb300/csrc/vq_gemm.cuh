@@ -596,10 +596,11 @@ __device__ __forceinline__ void consume_stage(uint32_t sb, uint32_t xsb,
       const float c_b = fmaf(-kOffset, s_b, bf16_of(bi1[r], jj));
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        tot[r][mt][0] = fmaf(s_a, acc[r][mt][0], fmaf(c_a, xs[mt].x, tot[r][mt][0]));
-        tot[r][mt][1] = fmaf(s_a, acc[r][mt][1], fmaf(c_a, xs[mt].y, tot[r][mt][1]));
-        tot[r][mt][2] = fmaf(s_b, acc[r][mt][2], fmaf(c_b, xs[mt].x, tot[r][mt][2]));
-        tot[r][mt][3] = fmaf(s_b, acc[r][mt][3], fmaf(c_b, xs[mt].y, tot[r][mt][3]));
+        // tot = s*acc + (c*xs + tot), two lanes per instruction
+        fma2(tot[r][mt][0], tot[r][mt][1], c_a, c_a, xs[mt].x, xs[mt].y);
+        fma2(tot[r][mt][0], tot[r][mt][1], s_a, s_a, acc[r][mt][0], acc[r][mt][1]);
+        fma2(tot[r][mt][2], tot[r][mt][3], c_b, c_b, xs[mt].x, xs[mt].y);
+        fma2(tot[r][mt][2], tot[r][mt][3], s_b, s_b, acc[r][mt][2], acc[r][mt][3]);
       }
     }
   });
@@ -864,10 +865,10 @@ __device__ __forceinline__ void consume_stage_xt(uint32_t sb, int kt, uint32_t T
     for (int r = 0; r < RT; ++r) {
       const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
       const float b_a = bf16_of(bi0[r], jj), b_b = bf16_of(bi1[r], jj);
-      tot[r][0][0] = fmaf(s_a, acc[r][0], fmaf(b_a, T0, tot[r][0][0]));
-      tot[r][0][1] = fmaf(s_a, acc[r][1], fmaf(b_a, T1, tot[r][0][1]));
-      tot[r][0][2] = fmaf(s_b, acc[r][2], fmaf(b_b, T0, tot[r][0][2]));
-      tot[r][0][3] = fmaf(s_b, acc[r][3], fmaf(b_b, T1, tot[r][0][3]));
+      fma2(tot[r][0][0], tot[r][0][1], b_a, b_a, T0, T1);
+      fma2(tot[r][0][0], tot[r][0][1], s_a, s_a, acc[r][0], acc[r][1]);
+      fma2(tot[r][0][2], tot[r][0][3], b_b, b_b, T0, T1);
+      fma2(tot[r][0][2], tot[r][0][3], s_b, s_b, acc[r][2], acc[r][3]);
     }
   });
 }
@@ -1074,10 +1075,10 @@ __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
       for (int r = 0; r < RT; ++r) {
         const float s_a = bf16_of(sc0[r], jj), s_b = bf16_of(sc1[r], jj);
         const float b_a = bf16_of(bi0[r], jj), b_b = bf16_of(bi1[r], jj);
-        part[r][mt][0] = fmaf(s_a, acc[r][mt][0], fmaf(b_a, T0, part[r][mt][0]));
-        part[r][mt][1] = fmaf(s_a, acc[r][mt][1], fmaf(b_a, T1, part[r][mt][1]));
-        part[r][mt][2] = fmaf(s_b, acc[r][mt][2], fmaf(b_b, T0, part[r][mt][2]));
-        part[r][mt][3] = fmaf(s_b, acc[r][mt][3], fmaf(b_b, T1, part[r][mt][3]));
+        fma2(part[r][mt][0], part[r][mt][1], b_a, b_a, T0, T1);
+        fma2(part[r][mt][0], part[r][mt][1], s_a, s_a, acc[r][mt][0], acc[r][mt][1]);
+        fma2(part[r][mt][2], part[r][mt][3], b_b, b_b, T0, T1);
+        fma2(part[r][mt][2], part[r][mt][3], s_b, s_b, acc[r][mt][2], acc[r][mt][3]);
       }
     });
   });
@@ -1087,10 +1088,8 @@ __device__ __forceinline__ void consume_stage_xs(uint32_t sb, const XsLane& o,
     const float i0 = __uint_as_float(iv.x), i1 = __uint_as_float(iv.y);
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
-      tot[r][mt][0] = fmaf(i0, part[r][mt][0], tot[r][mt][0]);
-      tot[r][mt][1] = fmaf(i1, part[r][mt][1], tot[r][mt][1]);
-      tot[r][mt][2] = fmaf(i0, part[r][mt][2], tot[r][mt][2]);
-      tot[r][mt][3] = fmaf(i1, part[r][mt][3], tot[r][mt][3]);
+      fma2(tot[r][mt][0], tot[r][mt][1], i0, i1, part[r][mt][0], part[r][mt][1]);
+      fma2(tot[r][mt][2], tot[r][mt][3], i0, i1, part[r][mt][2], part[r][mt][3]);
     }
   });
 }

@@ -662,11 +662,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float4* xs4 = reinterpret_cast<const float4*>(xs_base + j * MP + HC * ch);
 #pragma unroll
             for (int i4 = 0; i4 < HC / 4; ++i4) {
+              // tot = s*acc + (c*X_g + tot), two columns per instruction
               const float4 xs = xs4[i4];
-              tot[4 * i4 + 0] = fmaf(s, __uint_as_float(acc[4 * i4 + 0]), fmaf(c, xs.x, tot[4 * i4 + 0]));
-              tot[4 * i4 + 1] = fmaf(s, __uint_as_float(acc[4 * i4 + 1]), fmaf(c, xs.y, tot[4 * i4 + 1]));
-              tot[4 * i4 + 2] = fmaf(s, __uint_as_float(acc[4 * i4 + 2]), fmaf(c, xs.z, tot[4 * i4 + 2]));
-              tot[4 * i4 + 3] = fmaf(s, __uint_as_float(acc[4 * i4 + 3]), fmaf(c, xs.w, tot[4 * i4 + 3]));
+              fma2(tot[4 * i4 + 0], tot[4 * i4 + 1], c, c, xs.x, xs.y);
+              fma2(tot[4 * i4 + 0], tot[4 * i4 + 1], s, s, __uint_as_float(acc[4 * i4 + 0]),
+                   __uint_as_float(acc[4 * i4 + 1]));
+              fma2(tot[4 * i4 + 2], tot[4 * i4 + 3], c, c, xs.z, xs.w);
+              fma2(tot[4 * i4 + 2], tot[4 * i4 + 3], s, s, __uint_as_float(acc[4 * i4 + 2]),
+                   __uint_as_float(acc[4 * i4 + 3]));
             }
           }
         }
