@@ -16,9 +16,10 @@
 //     requested before anything else is done. The block's keys span at most
 //     two consecutive chunks, so each block owns at most one of them: it
 //     prefetches those rows of k_new and v_new at the start (up to 16 of
-//     them; more are loaded when the chunk comes), places them in
-//     the chunk's tile, rotates the keys at P + j there and, in row group 0,
-//     appends keys and values to slots S + j of the caches.
+//     them), rotates the keys at P + j and, in row group 0, appends keys and
+//     values to slots S + j of the caches there and then, and places them in
+//     the chunk's tile when that chunk comes (more than 16 rows: loaded,
+//     rotated and appended in the tile when the chunk comes).
 //   - Meanwhile the block loads the group's queries, rotates them at P + j and
 //     rounds them to the storage type (the (cos, sin) of up to 16 positions at
 //     a time in a shared table, the frequencies staged in shared memory).
@@ -429,9 +430,35 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
   cp_async_wait_all();
   __syncthreads();
   // the eight rows rotated at P + j in place (eight pairs per step when rh is
-  // a multiple of 8, else one)
+  // a multiple of 8, else one), and after them the prefetched block keys at
+  // P + jb0 + a in the staging rows (so that the chunk holding them only
+  // copies them into its tile)
+  const int nq_items = max(q_end - rr0 - q0, 0) * npc, nk_items = staged ? (jb1 - jb0) * npc : 0;
   if (rh > 0)
-    for (int i = tid; i < (q_end - rr0 - q0) * npc; i += kAttnThreads) {
+    for (int i = tid; i < nq_items + nk_items; i += kAttnThreads) {
+      if (i >= nq_items) {
+        const int a = (i - nq_items) / npc, u = (i - nq_items) - a * npc;
+        const uint32_t row = app + (uint32_t)(a * D * 2);
+        const uint32_t cs_row = tab + (uint32_t)(a * kMaxRotPairs) * 8u;
+        if (vec8) {
+          float2 cs[8];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint4 w = lds128(cs_row + (uint32_t)(8 * u + 2 * m) * 8u);
+            cs[2 * m] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+            cs[2 * m + 1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+          }
+          rot8<kF16>(row + 16u * (uint32_t)u, row + 2u * (uint32_t)(8 * u + rh), cs);
+        } else {
+          const uint32_t a1 = row + 2u * (uint32_t)u, a2 = row + 2u * (uint32_t)(u + rh);
+          float r1, r2;
+          rot_pair(h2f<kF16>(lds16(a1)), h2f<kF16>(lds16(a2)), lds64f(cs_row + (uint32_t)u * 8u),
+                   r1, r2);
+          sts16(a1, f2h<kF16>(r1));
+          sts16(a2, f2h<kF16>(r2));
+        }
+        continue;
+      }
       const int k = i / npc, u = i - k * npc;
       const int lr = q0 + k;
       const uint32_t cs_row = tabq + (uint32_t)(((rr0 + lr) / p.G - jq0) * kMaxRotPairs) * 8u;
@@ -454,6 +481,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
       }
     }
   __syncthreads();
+  // row group 0 appends the prefetched block keys (rotated) and values to
+  // slots S + jb0 .. of the caches: nothing in this call reads them back (the
+  // chunk that holds those keys takes them from the staging rows; a box that
+  // covers the slots is overwritten there)
+  if (staged && rg == 0)
+    for (int e = tid; e < (jb1 - jb0) * 2 * (D / 8); e += kAttnThreads) {
+      const int a = e / (2 * (D / 8)), rem = e - a * (2 * (D / 8));
+      const int kv = rem / (D / 8), c = rem - kv * (D / 8);
+      const uint4 v = lds128(app + (uint32_t)((kv * kAppRows + a) * D * 2 + c * 16));
+      const size_t dst = (head + (size_t)(S + jb0 + a)) * D + c * 8;
+      if (in_bounds(dst + 7, p.cache_elems, p.err))
+        *reinterpret_cast<uint4*>((kv ? p.v_cache : p.k_cache) + dst) = v;
+    }
   // the eight rows into every other block's query tile (the same offsets)
   cluster_wait();
   for (int i = tid; i < (kCluster - 1) * kMergeRows * (D / 8); i += kAttnThreads) {
@@ -553,7 +593,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
         cp_async_wait_all();
       }
       __syncthreads();   // block-uniform branch: the rows are in place
-      if (rh > 0) {
+      // (staged rows were rotated and appended at the start)
+      if (rh > 0 && !staged) {
         for (int e = tid; e < (n_vis - n_pre) * npc; e += kAttnThreads) {
           const int tl = n_pre + e / npc, u = e - (e / npc) * npc;
           if (vec8)
@@ -563,7 +604,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kAttnThreads,
         }
         __syncthreads();
       }
-      if (rg == 0)
+      if (rg == 0 && !staged)
         for (int e = tid; e < (n_vis - n_pre) * 2 * (D / 8); e += kAttnThreads) {
           const int tl = n_pre + e / (2 * (D / 8)), rem = e % (2 * (D / 8));
           const int kv = rem / (D / 8), c = rem - kv * (D / 8);
