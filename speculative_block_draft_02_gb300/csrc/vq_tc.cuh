@@ -29,11 +29,12 @@
 //                      tcgen05.mma kind::f16, M=128, N=MP,
 //                      K=16, A from TMEM, B (x) from shared memory, into one
 //                      of 4 fp32 accumulators in TMEM; tcgen05.commit.
-//   fold (16 warps)    per pair of groups, tcgen05.ld of both accumulators
-//                      (a row per lane, a quarter of the MP columns per
-//                      warp) and the fp32
-//                      fold with scale, bias and X_g; then the epilogue
-//                      (store y, or the running arg max).
+//   fold (16 warps, 8 in the projection at MP = 32)
+//                      per group, tcgen05.ld of its accumulator (a row per
+//                      lane, a quarter (half) of the MP columns per warp) and
+//                      the fp32 fold with scale, bias and X_g, two columns per
+//                      packed multiply-add; then the epilogue (store y, or
+//                      the running arg max).
 // X_g: a table for all of K in shared memory, written once per call by a
 // small kernel into the workspace and copied in (vq_linear), or summed by the
 // fold warps from each stage's x tile during the block's first unit (arg max,
@@ -49,11 +50,20 @@ namespace vq {
 #ifdef __CUDACC__
 
 constexpr int kTcUnpackWarps = 8;
-constexpr int kTcFoldWarps = 16;
-constexpr int kTcProducerWarp = kTcUnpackWarps + kTcFoldWarps;   // 24
-constexpr int kTcMmaWarp = kTcProducerWarp + 1;                   // 25, 26
 constexpr int kTcMmaWarps = 2;
-constexpr int kTcThreads = (kTcMmaWarp + kTcMmaWarps) * 32;       // 864
+// Warp roles of a block: unpack warps 0-7, then the fold warps, the producer
+// and the two MMA warps. Sixteen fold warps (each a lane quarter and a quarter
+// of the MP accumulator columns), except eight (half the columns each) for
+// the projection at MP = 32 — measured at K = 5120, N = 17408: M = 32 27.7 ->
+// 25.8 us with eight, while at MP = 64 and in the arg max sixteen stay faster
+// (32.3 against 34.7 us, 143 against 170 us).
+template <int MP, bool ARGMAX>
+struct TcRoles {
+  static constexpr int kFold = (MP == 32 && !ARGMAX) ? 8 : 16;
+  static constexpr int kProducer = kTcUnpackWarps + kFold;
+  static constexpr int kMma = kProducer + 1;
+  static constexpr int kThreads = (kMma + kTcMmaWarps) * 32;   // 864 (608 with 8 fold warps)
+};
 constexpr int kTcBufs = 4;              // A buffers and accumulators in flight
 constexpr uint32_t kTcTmemCols = 512;   // A: 4 x 32 columns, D: 4 x MP (<= 64) columns
 constexpr uint32_t kTcDCol = 32 * kTcBufs;   // first accumulator column
@@ -311,7 +321,7 @@ __device__ __forceinline__ void warp_top2_columns(float (&v)[HC], uint32_t (&n)[
 }
 
 template <int ACT, int MP, bool ARGMAX>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcRoles<MP, ARGMAX>::kThreads, 1)
     vq_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                  const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_x,
                  const GemmParams p) {
@@ -322,6 +332,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // made exact (one fp16 subtraction per pair) and c0 = 0.
   constexpr bool kExact = ARGMAX && kF16;
   constexpr float kC0 = kExact ? 0.f : kF16 ? 1024.f : 128.f;
+  constexpr int kTcFoldWarps = TcRoles<MP, ARGMAX>::kFold;
+  constexpr int kTcProducerWarp = TcRoles<MP, ARGMAX>::kProducer;
+  constexpr int kTcMmaWarp = TcRoles<MP, ARGMAX>::kMma;
   constexpr int HC = MP / (kTcFoldWarps / 4);   // accumulator columns per fold warp
   constexpr uint32_t kIdesc = tc_idesc(!kF16, MP);
   static_assert(MP == 32 || MP == 64, "MP");
@@ -761,7 +774,7 @@ int launch_tc(const GemmLaunch& L) {
                               L.p.x, L.p.M, L.p.K, L.p.KT, MP, (float*)L.p.xprep);
     if (rc != VQ_OK) return rc;
   }
-  return launch_pdl(k, dim3(L.grid), kTcThreads, L.smem, L.stream, L.tm_w, L.tm_s, L.tm_b, L.tm_x,
+  return launch_pdl(k, dim3(L.grid), TcRoles<MP, AM>::kThreads, L.smem, L.stream, L.tm_w, L.tm_s, L.tm_b, L.tm_x,
                     L.p);
 }
 
