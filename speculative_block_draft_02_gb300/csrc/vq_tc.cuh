@@ -540,10 +540,10 @@ __global__ void __launch_bounds__(TcRoles<MP, ARGMAX>::kThreads, 1)
             !wait_or_abort(full_bar(slot), (uint32_t)(q / p.D) & 1u, abort_flag, p.err))
           aborted = true;
         const uint32_t sb = base + slot * p.stage_bytes;
-        // unrolled only by two for the projection (14 % faster at M = 64 than
-        // fully unrolled: less code to fetch among the roles), fully for the
-        // arg max (1 % faster there)
-#pragma unroll(ARGMAX ? 4 : 2)
+        // unrolled only by two (the projection at M = 64 14 % faster than
+        // fully unrolled: less code to fetch among the roles; the arg max,
+        // with its fold loop unrolled by four, 1 % faster)
+#pragma unroll(2)
         for (int jj = 0; jj < 4; ++jj) {
           const int j = 2 * jj + par;
           const int G = 8 * q + j;
@@ -641,10 +641,12 @@ __global__ void __launch_bounds__(TcRoles<MP, ARGMAX>::kThreads, 1)
         const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
         // one group per step (buffer j & 3): its accumulator is read, the
         // buffer released, then folded (one group's HC registers at a time
-        // keeps the fold warps within their register budget). The arg max
-        // keeps this loop rolled (its larger epilogue already fills the
-        // instruction cache: 3 % faster measured), the projection unrolls it.
-#pragma unroll(ARGMAX ? 1 : 8)
+        // keeps the fold warps within their register budget). The projection
+        // unrolls this loop fully; the arg max, whose larger epilogue shares
+        // the instruction cache, by four (measured with the packed
+        // multiply-adds, per call: rolled 142.9 us, by two 137.8, by four
+        // 130.3, fully 138.1).
+#pragma unroll(ARGMAX ? 4 : 8)
         for (int j = 0; j < 8; ++j) {
           const int G = 8 * q + j;
           const int b = j & 3;
@@ -661,7 +663,7 @@ __global__ void __launch_bounds__(TcRoles<MP, ARGMAX>::kThreads, 1)
           if (lane == 0) mbar_arrive(dempty_bar(b));
           if (!aborted) {
             uint32_t s2, b2;
-            if constexpr (ARGMAX) {   // rolled loop: from shared memory, not indexed registers
+            if constexpr (ARGMAX) {   // from shared memory (fewer live registers)
               s2 = lds32_at(sb + kTcOffS + (uint32_t)nl * 16u + (uint32_t)(j >> 1) * 4u);
               b2 = lds32_at(sb + kTcOffB + (uint32_t)nl * 16u + (uint32_t)(j >> 1) * 4u);
             } else {
