@@ -29,7 +29,7 @@
 //                      tcgen05.mma kind::f16, M=128, N=MP,
 //                      K=16, A from TMEM, B (x) from shared memory, into one
 //                      of 4 fp32 accumulators in TMEM; tcgen05.commit.
-//   fold (16 warps, 8 in the projection at MP = 32)
+//   fold (16 warps, 8 at MP = 32)
 //                      per group, tcgen05.ld of its accumulator (a row per
 //                      lane, a quarter (half) of the MP columns per warp) and
 //                      the fp32 fold with scale, bias and X_g, two columns per
@@ -53,13 +53,14 @@ constexpr int kTcUnpackWarps = 8;
 constexpr int kTcMmaWarps = 2;
 // Warp roles of a block: unpack warps 0-7, then the fold warps, the producer
 // and the two MMA warps. Sixteen fold warps (each a lane quarter and a quarter
-// of the MP accumulator columns), except eight (half the columns each) for
-// the projection at MP = 32 — measured at K = 5120, N = 17408: M = 32 27.7 ->
-// 25.8 us with eight, while at MP = 64 and in the arg max sixteen stay faster
-// (32.3 against 34.7 us, 143 against 170 us).
+// of the MP accumulator columns) at MP = 64, eight (half the columns each) at
+// MP = 32 — measured: the projection at M = 32, K = 5120, N = 17408 27.7 ->
+// 25.8 us with eight, the arg max at M = 32, K = 2560, N = 151936 104.4 ->
+// 100.7 us; at MP = 64 sixteen stay faster (projection 32.3 against 34.7 us,
+// arg max 143 against 170 us).
 template <int MP, bool ARGMAX>
 struct TcRoles {
-  static constexpr int kFold = (MP == 32 && !ARGMAX) ? 8 : 16;
+  static constexpr int kFold = MP == 32 ? 8 : 16;
   static constexpr int kProducer = kTcUnpackWarps + kFold;
   static constexpr int kMma = kProducer + 1;
   static constexpr int kThreads = (kMma + kTcMmaWarps) * 32;   // 864 (608 with 8 fold warps)
