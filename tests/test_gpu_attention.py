@@ -124,6 +124,10 @@ CASES = [
     # a chunk that reaches the block near the cache end: its 64-row box of the
     # last KV head runs past the end of the cache tensor (zero-filled rows)
     (1, 8, 4, 2, 64, 100, [90], [92], "f16", 64, 1e4),
+    # rotary widths that are not multiples of 16 (one pair per rotation step,
+    # for the queries and for the prefetched block keys)
+    (2, 8, 4, 2, 64, 300, [100, 37], [120, 37], "f16", 40, 1e4),
+    (1, 16, 8, 2, 128, 200, [70], None, "bf16", 6, 1e4),
 ]
 
 

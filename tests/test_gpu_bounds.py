@@ -153,13 +153,15 @@ def test_verify_round_checked_build(checked):
 
 # (B, L, Hq, Hkv, D, S_cap, prefix_len, src_off, dtype, rotary_dim): the
 # full-size workload, two row groups, the block at the cache end (a key box
-# past the tensor's end), D=64 bf16, and rows out of range (flagged, skipped)
+# past the tensor's end), D=64 bf16, rows out of range (flagged, skipped), and
+# a rotary width that is not a multiple of 16 (one pair per rotation step)
 ATTN = [
     (4, 16, 32, 8, 128, 2048, None, None, "f16", 128),
     (2, 10, 16, 2, 64, 400, [5, 250], [260, 250], "f16", 64),
     (1, 8, 4, 2, 64, 100, [90], [92], "f16", 64),
     (2, 8, 4, 4, 64, 300, [129, 255], [200, 292], "bf16", 32),
     (4, 8, 8, 2, 128, 256, [40, 100, 10, 200], [60, 90, 248, 250], "f16", 64),
+    (2, 8, 4, 2, 64, 300, [100, 37], [120, 37], "f16", 40),
 ]
 
 
